@@ -1,0 +1,360 @@
+"""Pins for the CPU oracle: each check ties the oracle to something other than
+itself -- hand-worked values, exact rational arithmetic, library routines
+(numpy integer/fp64 matmul, numpy fp16, torch bf16 rounding), brute force and
+invariants.  None of these needs a GPU."""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from w4a16_linear_layers_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def torch_bf16_bits(values_f32: np.ndarray) -> np.ndarray:
+    """Library rounding fp32 -> bf16 (torch, round to nearest even)."""
+    t = torch.from_numpy(np.ascontiguousarray(values_f32, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_of(values) -> np.ndarray:
+    return torch_bf16_bits(np.asarray(values, np.float32))
+
+
+# ------------------------------------------------------------------ formats
+
+def test_f16_decode_all_patterns(oracle_lib):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = pats.view(np.float16).astype(np.float32)
+    got = np.array([oracle_lib.f16_to_f32(int(p)) for p in pats], np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_bf16_rounding_matches_torch(oracle_lib):
+    rng = np.random.default_rng(1)
+    vals = rng.standard_normal(20000).astype(np.float32) * np.float32(1000.0)
+    bits = vals.view(np.uint32)
+    # exact ties (lower 16 bits == 0x8000), both parities, plus carries into the exponent
+    ties = ((bits & np.uint32(0xFFFF0000)) | np.uint32(0x8000)).view(np.float32)
+    carry = np.array([0x3F7FFFFF, 0x3F7F8000, 0x477F8000, 0xBF7FC000], np.uint32).view(np.float32)
+    allv = np.concatenate([vals, ties[:5000], carry, np.float32([0.0, -0.0, 1e-40, -3e-39])])
+    ref = bf16_of(allv)
+    got = np.array([oracle_lib.f32_to_bf16(float(v)) for v in allv], np.uint16)
+    assert np.array_equal(got, ref)
+    back = np.array([oracle_lib.bf16_to_f32(int(b)) for b in ref[:1000]], np.float32)
+    assert np.array_equal(back.view(np.uint32), ref[:1000].astype(np.uint32) << 16)
+
+
+# --------------------------------------------------------------- act-quant
+
+def _read_act_golden():
+    rows = []
+    with open(os.path.join(GOLDEN, "act_quant_hand.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            xs, ss, qs = line.split("|")
+            x = [float(v) for v in xs.split(":")[1].split()]
+            s = float.fromhex(ss.split(":")[1].strip())
+            q = [int(v) for v in qs.split(":")[1].split()]
+            rows.append((x, s, q))
+    return rows
+
+
+def test_act_quant_hand_rows(oracle_lib):
+    for x, s, q in _read_act_golden():
+        xb = bf16_of(x)[None, :]
+        assert np.array_equal(synth.bf16_values(xb)[0], np.float32(x)), "fixture not exact in bf16"
+        gq, gs = oracle_lib.act_quant_i8(xb)
+        assert gs[0] == np.float32(s)
+        assert gq[0].tolist() == q
+
+
+def _rn32(v: Fraction) -> Fraction:
+    """Exact round-to-nearest-even of a rational to binary32 (normal range)."""
+    if v == 0:
+        return Fraction(0)
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    ulp = Fraction(2) ** (e - 23)
+    t = a / ulp
+    fl = t.numerator // t.denominator
+    rem = t - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * fl * ulp
+
+
+def _rint_even(v: Fraction) -> int:
+    fl = v.numerator // v.denominator
+    rem = v - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return fl
+
+
+def test_act_quant_exact_rational(oracle_lib):
+    """Every q equals rint(RN32(x / RN32(amax / 127))) evaluated in exact
+    rational arithmetic (round half to even at both steps)."""
+    M, K = 6, 512
+    xb = synth.activations(11, "pin/act", M, K, "outliers")
+    q, s = oracle_lib.act_quant_i8(xb)
+    x = synth.bf16_values(xb)
+    for m in range(M):
+        amax = Fraction(float(np.max(np.abs(x[m]))))
+        sm = _rn32(amax / 127)
+        assert Fraction(float(s[m])) == sm
+        for k in range(K):
+            xv = Fraction(float(x[m, k]))
+            want = max(-127, min(127, _rint_even(_rn32(xv / sm))))
+            assert int(q[m, k]) == want, (m, k)
+
+
+def test_act_quant_divide_not_reciprocal(oracle_lib):
+    """Search for an element whose x/s and x*(127/amax) round to different
+    integers; the oracle must follow the IEEE divide (checked exactly)."""
+    found = None
+    for trial in range(200):
+        xb = synth.activations(100 + trial, "pin/divform", 1, 1024, "normal")
+        x = synth.bf16_values(xb)[0]
+        amax = np.float32(np.max(np.abs(x)))
+        sf = np.float32(amax / np.float32(127.0))
+        div = np.rint(x / sf)
+        mul = np.rint(x * (np.float32(127.0) / amax))
+        idx = np.nonzero(div != mul)[0]
+        if idx.size:
+            found = (xb, int(idx[0]))
+            break
+    assert found is not None, "no divide-sensitive element found"
+    xb, k = found
+    q, s = oracle_lib.act_quant_i8(xb)
+    x = synth.bf16_values(xb)[0]
+    sm = _rn32(Fraction(float(np.max(np.abs(x)))) / 127)
+    assert int(q[0, k]) == _rint_even(_rn32(Fraction(float(x[k])) / sm))
+
+
+def test_act_quant_invariants(oracle_lib):
+    M, K = 16, 1024
+    for kind in ("outliers", "normal", "silu_mul", "normal2"):
+        xb = synth.activations(3, "pin/inv/" + kind, M, K, kind)
+        q, s = oracle_lib.act_quant_i8(xb)
+        x = synth.bf16_values(xb).astype(np.float64)
+        sd = s.astype(np.float64)[:, None]
+        assert np.all(np.abs(q.astype(np.int32)) <= 127)
+        assert np.all(np.max(np.abs(q.astype(np.int32)), axis=1) == 127)
+        # |x/s - q| <= 1/2 up to the rounding of the fp32 quotient
+        err = np.abs(x / sd - q)
+        assert np.all(err <= 0.5 + 127 * 2.0**-23)
+
+
+def test_act_quant_zero_and_tiny_rows(oracle_lib):
+    xb = np.zeros((3, 256), np.uint16)
+    xb[1, 7] = bf16_of([1e-30])[0]          # tiny but normal
+    xb[2, :] = bf16_of(np.full(256, -3.0))
+    q, s = oracle_lib.act_quant_i8(xb)
+    assert s[0] == 0 and not q[0].any()
+    assert q[1, 7] == 127 and np.count_nonzero(q[1]) == 1
+    assert np.all(q[2] == -127)
+
+
+# -------------------------------------------------------------------- pack
+
+def _read_pack_golden():
+    out = []
+    with open(os.path.join(GOLDEN, "pack_words.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            b, qs, w = line.split("|")
+            out.append((int(b), [int(v) for v in qs.split()], int(w.strip(), 16)))
+    return out
+
+
+def test_pack_hand_words(oracle_lib):
+    for bits, qs, word in _read_pack_golden():
+        per = 32 // bits
+        q = np.zeros((128, 8), np.int8)
+        q[:per, 1] = qs
+        qw, qz, bad = oracle_lib.pack_gptq(q, bits)
+        assert bad == 0
+        assert int(qw[0, 1]) & 0xFFFFFFFF == word
+        zero_word = 0x80808080 if bits == 8 else 0x88888888
+        assert np.all(qz.view(np.uint32) == zero_word)
+        assert int(qw[0, 0]) & 0xFFFFFFFF == zero_word
+
+
+def test_pack_roundtrip_and_range(oracle_lib):
+    for bits, lo, hi in ((8, -128, 127), (4, -8, 7)):
+        q = synth.randint(5, f"pin/pack{bits}", (512, 40), lo, hi, np.int8)
+        qw, qz, bad = oracle_lib.pack_gptq(q, bits)
+        assert bad == 0 and qw.shape == (512 * bits // 32, 40)
+        assert np.array_equal(oracle_lib.unpack_gptq(qw, 512, 40, bits), q)
+        # an independent numpy unpack of the same words
+        per = 32 // bits
+        u = qw.view(np.uint32)
+        ref = np.empty_like(q)
+        for i in range(per):
+            ref[i::per] = ((u >> np.uint32(bits * i)) & np.uint32((1 << bits) - 1)).astype(np.int32) - (1 << (bits - 1))
+        assert np.array_equal(ref, q)
+    q = np.zeros((128, 4), np.int8)
+    q[3, 2] = 9        # outside int4
+    q[5, 1] = -9
+    _, _, bad = oracle_lib.pack_gptq(q, 4)
+    assert bad == 2
+
+
+# ------------------------------------------------------------------ W8A8
+
+def test_group_partials_brute_force_all_pairs(oracle_lib):
+    """All 255^2 (a, w) pairs on a 128-long group: P = 128 * a * w."""
+    vals = np.arange(-127, 128, dtype=np.int8)
+    qa = np.repeat(vals[:, None], 128, axis=1)            # row i constant a_i
+    qwt = np.repeat(vals[None, :], 128, axis=0)          # column j constant w_j
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    P = oracle_lib.group_partials_i8(qa, qw, 128)
+    want = 128 * vals.astype(np.int64)[:, None] * vals.astype(np.int64)[None, :]
+    assert P.shape == (1, 255, 255)
+    assert np.array_equal(P[0].astype(np.int64), want)
+
+
+def test_group_partials_vs_numpy_matmul(oracle_lib):
+    M, K, N = 5, 640, 33
+    qa = synth.randint(7, "pin/gp/a", (M, K), -127, 127)
+    qwt = synth.randint(7, "pin/gp/w", (K, N), -127, 127)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    P = oracle_lib.group_partials_i8(qa, qw, K)
+    for g in range(K // 128):
+        sl = slice(128 * g, 128 * (g + 1))
+        ref = qa[:, sl].astype(np.int64) @ qwt[sl].astype(np.int64)
+        assert np.array_equal(P[g].astype(np.int64), ref)
+    # extreme magnitudes: all +-127 stays exact and within int32
+    qa2 = np.full((2, 128), 127, np.int8)
+    qa2[1] = -127
+    qw2, _, _ = oracle_lib.pack_gptq(np.full((128, 2), -127, np.int8), 8)
+    P2 = oracle_lib.group_partials_i8(qa2, qw2, 128)
+    assert P2[0, 0, 0] == -128 * 127 * 127 and P2[0, 1, 1] == 128 * 127 * 127
+
+
+def test_w8a8_hand_fixture(oracle_lib):
+    rows = []
+    with open(os.path.join(GOLDEN, "w8a8_hand.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            c, ps, yf, yb = line.split("|")
+            rows.append((int(c), [int(v) for v in ps.split()], float(yf), int(yb.strip(), 16)))
+    K = 256
+    qa = np.ones((1, K), np.int8)
+    qa[0, 128:] = -1
+    qwt = np.zeros((K, 2), np.int8)
+    qwt[:128, 0], qwt[128:, 0] = 2, 3
+    qwt[:128, 1], qwt[128:, 1] = -127, 127
+    sw = np.array([[0.5, 2.0**-7], [0.25, 1.0]])
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    out = oracle_lib.gemm_w8a8_gs128(qa, np.float32([0.25]), qw, synth.f16_bits(sw), K)
+    P = oracle_lib.group_partials_i8(qa, qw, K)
+    for c, ps, yf, yb in rows:
+        assert [int(P[0, 0, c]), int(P[1, 0, c])] == ps
+        assert out["y_f32"][0, c] == np.float32(yf)
+        assert int(out["y_bf16"][0, c]) == yb
+
+
+def test_w8a8_unit_scales_is_integer_matmul(oracle_lib):
+    """All scales 1: y = bf16(integer matmul), exact in fp32 for these sizes."""
+    M, K, N = 7, 384, 19
+    qa = synth.randint(9, "pin/unit/a", (M, K), -127, 127)
+    qwt = synth.randint(9, "pin/unit/w", (K, N), -127, 127)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    ones = np.full((K // 128, N), 0x3C00, np.uint16)       # fp16 1.0
+    out = oracle_lib.gemm_w8a8_gs128(qa, np.ones(M, np.float32), qw, ones, K)
+    ref = qa.astype(np.int64) @ qwt.astype(np.int64)
+    assert np.all(np.abs(ref) < 2**24)
+    assert np.array_equal(out["y_f32"], ref.astype(np.float32))
+    assert np.array_equal(out["y_bf16"], bf16_of(ref.astype(np.float32)))
+
+
+def test_w8a8_fp64_invariant(oracle_lib):
+    """y64 is the dequantize-then-fp64-matmul value (numpy route from the
+    generator's unpacked weights) and the fp32 chain lies within the bound."""
+    M, K, N = 9, 1280, 70
+    xb = synth.activations(21, "pin/f64/x", M, K, "outliers")
+    qa, sa = oracle_lib.act_quant_i8(xb)
+    qwt, swb = synth.w8a8_weights(21, "pin/f64/w", K, N)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    out = oracle_lib.gemm_w8a8_gs128(qa, sa, qw, swb, K)
+    sw = swb.view(np.float16).astype(np.float64)
+    w_dq = qwt.astype(np.float64) * np.repeat(sw, 128, axis=0)
+    a_dq = qa.astype(np.float64) * sa.astype(np.float64)[:, None]
+    ref = a_dq @ w_dq
+    assert np.allclose(out["y64"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert np.all(np.abs(out["y_f32"].astype(np.float64) - out["y64"]) <= out["bound"])
+    # bf16 output is the round-to-nearest-even image of the fp32 chain
+    assert np.array_equal(out["y_bf16"], bf16_of(out["y_f32"]))
+    # sub-grid evaluation agrees with the full one
+    rows, cols = np.array([8, 0, 3]), np.array([69, 1, 40])
+    sub = oracle_lib.gemm_w8a8_gs128(qa, sa, qw, swb, K, rows, cols)
+    assert np.array_equal(sub["y_bf16"], out["y_bf16"][np.ix_(rows, cols)])
+
+
+def test_w8a8_identity_probe(oracle_lib):
+    """Identity probe: feeding I_K through the W8A8 linear recovers q*s
+    within two fp32 roundings (plus the bf16 output rounding)."""
+    K, N = 256, 24
+    xb = bf16_of(np.eye(K, dtype=np.float32))
+    qa, sa = oracle_lib.act_quant_i8(xb)
+    assert np.all(np.diag(qa) == 127) and np.count_nonzero(qa) == K
+    qwt, swb = synth.w8a8_weights(4, "pin/probe8", K, N)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    out = oracle_lib.gemm_w8a8_gs128(qa, sa, qw, swb, K)
+    w_dq = qwt.astype(np.float64) * np.repeat(swb.view(np.float16).astype(np.float64), 128, axis=0)
+    assert np.all(np.abs(out["y_f32"] - w_dq) <= 2.0**-21 * np.abs(w_dq))
+
+
+# ----------------------------------------------------------------- W4A16
+
+def test_w4a16_identity_probe_bit_exact(oracle_lib):
+    """Identity probe: y = bf16(q * s) exactly (library rounding of the exact
+    fp32 product)."""
+    K, N = 256, 40
+    qwt, sb = synth.w4a16_weights(8, "pin/probe4", K, N)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 4)
+    xb = bf16_of(np.eye(K, dtype=np.float32))
+    out = oracle_lib.gemm_w4a16_g128(xb, qw, sb, K)
+    s = np.repeat(synth.bf16_values(sb), 128, axis=0)
+    want = bf16_of(qwt.astype(np.float32) * s)
+    assert np.array_equal(out["y_bf16"], want)
+    assert np.array_equal(oracle_lib.dequant_w4a16(qw, sb, K, N), want)
+
+
+def test_w4a16_unit_scales_integer(oracle_lib):
+    M, K, N = 4, 512, 9
+    x_int = synth.randint(12, "pin/w4unit/x", (M, K), -3, 3).astype(np.float32)
+    xb = bf16_of(x_int)
+    qwt = synth.randint(12, "pin/w4unit/w", (K, N), -8, 7)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 4)
+    ones = np.full((K // 128, N), 0x3F80, np.uint16)      # bf16 1.0
+    out = oracle_lib.gemm_w4a16_g128(xb, qw, ones, K)
+    ref = x_int.astype(np.int64) @ qwt.astype(np.int64)
+    assert np.array_equal(out["y_f32"], ref.astype(np.float32))
+
+
+def test_w4a16_fp64_invariant(oracle_lib):
+    M, K, N = 6, 1152, 50
+    xb = synth.activations(13, "pin/w4f64/x", M, K, "normal")
+    qwt, sb = synth.w4a16_weights(13, "pin/w4f64/w", K, N)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 4)
+    out = oracle_lib.gemm_w4a16_g128(xb, qw, sb, K)
+    s = np.repeat(synth.bf16_values(sb), 128, axis=0)
+    w = synth.bf16_values(bf16_of(qwt.astype(np.float32) * s)).astype(np.float64)
+    ref = synth.bf16_values(xb).astype(np.float64) @ w
+    assert np.allclose(out["y64"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert np.all(np.abs(out["y_f32"].astype(np.float64) - out["y64"]) <= out["bound"])
+    assert np.array_equal(out["y_bf16"], bf16_of(out["y_f32"]))
