@@ -1,0 +1,541 @@
+"""Benchmark of the group-wise quantized linear layer on GB300.
+
+Default workload (one JSON line on stdout): one DFlash2 drafter layer's seven
+W8A8 GS128 projections (q 5120->4096, k/v 5120->1024, o 4096->5120, gate/up
+5120->17408, down 17408->5120) at M = 8*C tokens for C in {1, 8, 12}
+(M = 8, 64, 96).  One step = for each M: dynamic INT8 quantization of the
+four distinct layer inputs, then the seven GEMMs (12 + 21 kernel launches),
+replayed as one CUDA graph.  Metric: weight GB/s (qweight + scale bytes
+streamed per step / step time); TOPS is reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload layer|single|drafter|w4a16|prefill|vocab]
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (the layer has no exchange step on one GPU);
+value = total over ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ workloads
+
+def workload_specs(name: str):
+    """List of (linear name, K, N, activation kind, M, kind 'w8a8'|'w4a16')."""
+    from w4a16_linear_layers_gb300 import synth
+
+    specs = []
+    if name == "layer":
+        for M in (8, 64, 96):
+            for lname, K, N, kind in synth.DRAFTER_LAYER:
+                specs.append((f"layers.0.{lname}", K, N, kind, M, "w8a8"))
+    elif name == "single":
+        specs.append(("single", 5120, 1024, "outliers", 8, "w8a8"))
+    elif name == "drafter":
+        for lname, K, N, kind in synth.drafter_linears():
+            specs.append((lname, K, N, kind, 96, "w8a8"))
+    elif name == "w4a16":
+        for M in (8, 64):
+            for lname, K, N, kind in synth.drafter_linears():
+                specs.append((lname, K, N, "normal", M, "w4a16"))
+    elif name == "prefill":
+        for M in (128, 512, 2048, 8192):
+            specs.append(("layers.0.gate_proj", 5120, 17408, "outliers", M, "w8a8"))
+            specs.append(("layers.0.up_proj", 5120, 17408, "outliers", M, "w8a8"))
+            specs.append(("layers.0.down_proj", 17408, 5120, "silu_mul", M, "w8a8"))
+    elif name == "vocab":
+        for M in (8, 96):
+            specs.append(("lm_head", 5120, 248320, "outliers", M, "w8a8"))
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    return specs
+
+
+WORKLOAD_DESC = {
+    "layer": "drafter layer: 7 W8A8 GS128 linears x M in {8,64,96}",
+    "single": "single W8A8 GS128 linear 5120->1024, M=8",
+    "drafter": "full drafter: 35 W8A8 GS128 linears + fc 25600->5120, M=96",
+    "w4a16": "full drafter in W4A16 g128 (36 linears), M in {8,64}",
+    "prefill": "W8A8 GS128 gate/up 5120->17408 + down 17408->5120, M in {128,512,2048,8192}",
+    "vocab": "W8A8 GS128 vocab head 5120->248320, M in {8,96}",
+}
+
+
+def weight_bytes(K, N, kind):
+    return (K * N if kind == "w8a8" else K * N // 2) + 2 * (K // 128) * N
+
+
+def gemm_algo_bytes(M, K, N, kind):
+    """Algorithmic bytes of one GEMM launch: weights + scales once, the
+    activation operand once (int8 for W8A8, bf16 for W4A16), activation
+    scales, and the bf16 output."""
+    act = M * K * (1 if kind == "w8a8" else 2) + (4 * M if kind == "w8a8" else 0)
+    return weight_bytes(K, N, kind) + act + 2 * M * N
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ---------------------------------------------------------------- our arm
+
+class LayerRunner:
+    """Device-resident weights and inputs for a workload, and one step."""
+
+    def __init__(self, specs, device, seed=0):
+        import torch
+
+        from w4a16_linear_layers_gb300 import qlin, synth
+
+        self.torch, self.qlin = torch, qlin
+        self.specs = specs
+        self.device = device
+        self.ws = qlin.Workspace(device)
+        self.weights = {}
+        self.inputs = {}
+        self.acts = {}
+        self.outputs = []
+        for name, K, N, kind, M, wk in specs:
+            key = (name, wk)
+            if key not in self.weights:
+                if wk == "w8a8":
+                    q, s = synth.w8a8_weights(seed, name, K, N)
+                    qd = torch.from_numpy(q).to(device)
+                    qw, _ = qlin.pack_gptq(qd, 8, with_qzeros=False)
+                    sd = torch.from_numpy(s.view(np.int16)).view(torch.float16).to(device)
+                else:
+                    q, s = synth.w4a16_weights(seed, name + "/w4", K, N)
+                    qd = torch.from_numpy(q).to(device)
+                    qw, _ = qlin.pack_gptq(qd, 4, with_qzeros=False)
+                    sd = torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).to(device)
+                del qd
+                self.weights[key] = (qw, sd)
+            ikey = (synth.shared_input_name(name), M, K, kind)
+            if ikey not in self.inputs:
+                xb = synth.activations(seed, f"{ikey[0]}/M{M}", M, K, kind)
+                self.inputs[ikey] = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(device)
+                if wk == "w8a8":
+                    self.acts[ikey] = (torch.empty((M, K), dtype=torch.int8, device=device),
+                                       torch.empty((M,), dtype=torch.float32, device=device))
+            self.outputs.append(torch.empty((M, N), dtype=torch.bfloat16, device=device))
+            self.ws.get(M, N, K)
+        torch.cuda.synchronize()
+        self.weight_bytes = sum(weight_bytes(K, N, wk) for _, K, N, _, _, wk in specs)
+        self.ops = sum(2 * M * K * N for _, K, N, _, M, _ in specs)
+        self.gemm_bytes = sum(gemm_algo_bytes(M, K, N, wk) for _, K, N, _, M, wk in specs)
+        self.n_actq = len(self.acts)
+        self.n_gemm = len(specs)
+
+    def _ikey(self, spec):
+        from w4a16_linear_layers_gb300 import synth
+
+        name, K, N, kind, M, wk = spec
+        return (synth.shared_input_name(name), M, K, kind)
+
+    def quantize(self):
+        for ikey, (q, s) in self.acts.items():
+            self.qlin.act_quant_i8(self.inputs[ikey], q, s)
+
+    def gemms(self):
+        ws = self.ws.buf
+        for spec, y in zip(self.specs, self.outputs):
+            name, K, N, kind, M, wk = spec
+            qw, sc = self.weights[(name, wk)]
+            ikey = self._ikey(spec)
+            if wk == "w8a8":
+                q, s = self.acts[ikey]
+                self.qlin.gemm_w8a8_gs128(q, s, qw, sc, y, workspace=ws)
+            else:
+                self.qlin.gemm_w4a16_g128(self.inputs[ikey], qw, sc, y, workspace=ws)
+
+    def step(self):
+        self.quantize()
+        self.gemms()
+
+    def capture(self, fn):
+        torch = self.torch
+        s = torch.cuda.Stream(self.device)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()              # warm the launch path (attributes, tensor maps)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+
+def time_graph(torch, graph, reps):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(reps):
+        graph.replay()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3  # seconds
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from w4a16_linear_layers_gb300 import build as qbuild
+    from w4a16_linear_layers_gb300 import qlin
+
+    qbuild.build()
+    device = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(device)
+    specs = workload_specs(args.workload)
+    runner = LayerRunner(specs, device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    step_graph = runner.capture(runner.step)
+    gemm_graph = runner.capture(runner.gemms)
+    for _ in range(args.warmup):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    st = qlin.device_status()
+    if st != qlin.QLIN_OK:
+        raise SystemExit(f"device status after warm-up: {qlin.status_string(st)}")
+
+    clocks = ClockSampler(local_rank)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_step = time_graph(torch, step_graph, args.steps)
+    t_gemm = time_graph(torch, gemm_graph, args.steps)
+    clock_info = clocks.stop()
+    if dist:
+        t = torch.tensor([t_step, t_gemm], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step, t_gemm = t.tolist()
+
+    # end to end through the binding: inputs copied from pinned host memory,
+    # outputs copied back, every step, no graph
+    host_in = {k: v.cpu().pin_memory() for k, v in runner.inputs.items()}
+    host_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in runner.outputs]
+    h2d = sum(v.numel() * 2 for v in host_in.values())
+    d2h = sum(y.numel() * 2 for y in runner.outputs)
+
+    def e2e_step():
+        for k, v in host_in.items():
+            runner.inputs[k].copy_(v, non_blocking=True)
+        runner.step()
+        for h, y in zip(host_out, runner.outputs):
+            h.copy_(y, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_reps = max(3, min(args.steps, 50))
+    t0 = time.perf_counter()
+    for _ in range(e2e_reps):
+        e2e_step()
+    torch.cuda.synchronize()
+    t_e2e = (time.perf_counter() - t0) / e2e_reps
+    if dist:
+        t = torch.tensor([t_e2e], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_e2e = t.item()
+    st = qlin.device_status()
+    if st != qlin.QLIN_OK:
+        raise SystemExit(f"device status after timing: {qlin.status_string(st)}")
+
+    if rank != 0:
+        return None
+    ms = t_step / args.steps * 1e3
+    value = runner.weight_bytes * args.steps * world / t_step / 1e9
+    hbm, bf16, peak_src = measured_peaks()
+    gemm_avg_s = t_gemm / (args.steps * runner.n_gemm)
+    bytes_per_launch = runner.gemm_bytes / runner.n_gemm
+    achieved = bytes_per_launch / gemm_avg_s / 1e9
+    line = {
+        "metric": "W8A8-GS128 linear weight GB/s (TOPS beside it); % of HBM roofline",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8xint8->fp32 (exact on fp16 tcgen05), bf16 out",
+        "data": "synthetic (seeded splitmix64; weights uniform int8, fp16 log-uniform scales)",
+        "config": {
+            "workload": WORKLOAD_DESC[args.workload],
+            "linears_per_step": runner.n_gemm,
+            "act_quant_per_step": runner.n_actq,
+            "weight_bytes_per_step": runner.weight_bytes,
+            "tops": round(runner.ops * args.steps * world / t_step / 1e12, 3),
+            "l2": "inputs larger than L2: each step streams its weight bytes once; "
+                  "no matrix is re-read before the others have passed through",
+            "timing": "CUDA graph of one step, CUDA events on the replay stream",
+            "parallelism": f"replicas x{world}",
+        },
+        "gpu_launches": (runner.n_actq + runner.n_gemm) * args.steps,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "qlin_gemm_kernel (W8A8 GS128)",
+            "achieved": round(achieved, 1),
+            "peak": hbm,
+            "peak_source": peak_src,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm, 4),
+            "traffic": None,
+            "bytes_per_launch": round(bytes_per_launch),
+            "avg_launch_us": round(gemm_avg_s * 1e6, 3),
+        },
+        "e2e": {
+            "value": round(runner.weight_bytes * world / t_e2e / 1e9, 2),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(t_e2e * 1e3, 4),
+        },
+        "clocks": clock_info,
+    }
+    return line, runner
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_sample(specs, budget_s, seed=0, cache=None):
+    """Time the oracle on a bounded sample of the workload: for every linear
+    of the step, the same fraction of its output columns (all rows), run on
+    all host cores (one thread per column slice; the C oracle runs without the
+    GIL).  Returns (weight bytes covered, seconds, threads, description)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    from w4a16_linear_layers_gb300 import synth
+
+    oracle.build()
+    nthreads = cores()
+    cache = {} if cache is None else cache
+
+    def operands(name, K, N, kind, M, wk, nc):
+        key = (name, wk)
+        if key not in cache:
+            if wk == "w8a8":
+                cache[key] = synth.w8a8_weights(seed, name, K, N)
+            else:
+                cache[key] = synth.w4a16_weights(seed, name + "/w4", K, N)
+        q, s = cache[key]
+        q, s = np.ascontiguousarray(q[:, :nc]), np.ascontiguousarray(s[:, :nc])
+        xb = synth.activations(seed, f"{synth.shared_input_name(name)}/M{M}", M, K, kind)
+        if wk == "w8a8":
+            qw, _, _ = oracle.pack_gptq(q, 8)
+            qa, sa = oracle.act_quant_i8(xb)
+            return (lambda ch, a=(qa, sa, qw, s, K): oracle.gemm_w8a8_gs128(*a, cols=ch))
+        qw, _, _ = oracle.pack_gptq(q, 4)
+        return (lambda ch, a=(xb, qw, s, K): oracle.gemm_w4a16_g128(*a, cols=ch))
+
+    def run(frac):
+        total_bytes = 0
+        tasks = []
+        for name, K, N, kind, M, wk in specs:
+            nc = max(1, int(round(N * frac)))
+            total_bytes += weight_bytes(K, nc, wk)
+            fn = operands(name, K, N, kind, M, wk, nc)
+            for ch in np.array_split(np.arange(nc), min(nthreads, nc)):
+                if ch.size:
+                    tasks.append((fn, ch))
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(nthreads) as ex:
+            list(ex.map(lambda t: t[0](t[1]), tasks))
+        return total_bytes, time.perf_counter() - t0
+
+    frac = 0.001
+    while True:                       # calibrate the sample size on this host
+        _, t = run(frac)
+        if t >= 0.2 * budget_s or frac >= 1.0:
+            break
+        frac = min(1.0, frac * min(16.0, max(2.0, 0.3 * budget_s / max(t, 1e-3))))
+    frac = min(1.0, frac * budget_s / max(t, 1e-3))
+    b, t = run(frac)
+    desc = (f"oracle on {frac * 100:.3f}% of the output columns of every linear of the step "
+            f"(all rows), {nthreads} threads")
+    return b, t, nthreads, desc
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    specs = workload_specs(args.workload)
+    per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    cache = {}
+    for _ in range(args.warmup):
+        oracle_sample(specs, min(per_step_budget, 2.0), cache=cache)
+    tot_b, tot_t = 0, 0.0
+    desc, thr = "", 1
+    for _ in range(args.steps):
+        b, t, thr, desc = oracle_sample(specs, per_step_budget, cache=cache)
+        tot_b += b
+        tot_t += t
+    value = tot_b / tot_t / 1e9
+    return {
+        "impl": "reference",
+        "metric": "W8A8-GS128 linear weight GB/s (TOPS beside it); % of HBM roofline",
+        "value": round(value, 6),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8xint8->int64 exact, fp32 rescale chain (CPU oracle)",
+        "data": "synthetic (seeded splitmix64)",
+        "config": {"workload": WORKLOAD_DESC[args.workload]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": thr,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# -------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="layer", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    out = run_ours(args, rank, world, local_rank)
+    if out is not None:
+        line, runner = out
+        b, t, thr, desc = oracle_sample(runner.specs, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(b / t / 1e9, 6), "unit": "GB/s", "cores": thr,
+                                "kind": "oracle", "sample": desc}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

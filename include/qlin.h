@@ -1,0 +1,205 @@
+/*
+ * qlin.h -- C ABI of libqlin, group-wise quantized linear layers for GB300.
+ *
+ * The library implements the quantized linear layer used to serve quantized
+ * block-diffusion drafters and their targets:
+ *
+ *   1. dynamic per-token symmetric INT8 activation quantization,
+ *   2. a W8A8 GEMM against GPTQ-packed symmetric INT8 weights with one fp16
+ *      scale per 128-wide K group (GS128),
+ *   3. the W4A16 g128 symmetric weight-only GEMM with bf16 activations,
+ *   4. the GPTQ packer that produces the weight format of 2 and 3.
+ *
+ * Format (all calls): GPTQ qweight / qzeros / scales, no g_idx,
+ * desc_act = false, symmetric, groups of exactly 128 contiguous K
+ * ("Flint-DFlash2-GPTQ-INT8-PTQR" model card, parameter table and the text
+ * under it; "Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card, property table).
+ * There is no zero-point input and no bias: qzeros is produced by the packer
+ * for format fidelity only and is never read.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or retains them.  All matrices are dense row-major.
+ *  - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and returns a qlin_status_t at launch time.  Errors found
+ *    on the device (a bounded wait that ran out, a packer input out of range)
+ *    are recorded in a device-wide error word and reported by
+ *    qlin_device_status().
+ *  - No exception crosses the ABI and nothing is printed.
+ *  - Shapes: M = tokens (rows of the activation), K = input features,
+ *    N = output features.  K must be a positive multiple of 128, N a positive
+ *    multiple of 8, M >= 0 (M == 0 is a no-op), and M, N, K <= 2^31 - 1.
+ *  - Alignment: every pointer must be 16-byte aligned (the kernels move data
+ *    with TMA and 16-byte vector accesses).
+ *  - The calls run only on an sm_103 GPU (GB300); elsewhere they return
+ *    QLIN_ERR_DEVICE.
+ */
+#ifndef QLIN_H
+#define QLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int qlin_status_t;
+
+#define QLIN_OK                   0
+#define QLIN_ERR_NULL            -1   /* a required pointer is NULL */
+#define QLIN_ERR_SHAPE           -2   /* M, N or K outside the rules above */
+#define QLIN_ERR_ALIGN           -3   /* a pointer is not 16-byte aligned */
+#define QLIN_ERR_WORKSPACE       -4   /* workspace NULL or smaller than qlin_workspace_bytes() */
+#define QLIN_ERR_BITS            -5   /* bits is not 4 or 8 */
+#define QLIN_ERR_DEVICE          -6   /* the current device is not an sm_103 GPU */
+#define QLIN_ERR_CUDA           -10   /* a CUDA runtime call or kernel launch failed */
+#define QLIN_ERR_DEVICE_TIMEOUT -20   /* a bounded wait inside a kernel ran out (device error word) */
+#define QLIN_ERR_VALUE_RANGE    -21   /* the packer met a value outside the bit width (device error word) */
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *qlin_stream_t;
+
+/*
+ * Dynamic per-token symmetric INT8 activation quantization.
+ *
+ * Passages: "Flint-DFlash2-GPTQ-INT8-PTQR" card, PTQR paragraph ("dynamic
+ * per-token activation quantization") and the serving recipe
+ * (VLLM_GFX908_ACT_QUANT=round); "Qwen3.8-27B-GPTQ-INT8-W8A8-GS128-PTQR"
+ * card, "Serving" (GEMM inputs are dynamically quantized to INT8).
+ *
+ * For each row m of x:  amax = max_k |x[m,k]|,  s_a[m] = amax / 127 (fp32,
+ * IEEE divide),  q[m,k] = rint(x[m,k] / s_a[m]) (fp32 IEEE divide, ties to
+ * even), clamped to [-127, 127].  A row of zeros gives s_a = 0 and q = 0.
+ * Non-finite inputs are outside the contract.
+ *
+ *   x    bf16 [M, K]   input activations
+ *   q    int8 [M, K]   output, quantized activations
+ *   s_a  fp32 [M]      output, per-token scales
+ */
+qlin_status_t qlin_act_quant_i8(const uint16_t *x, int64_t M, int64_t K,
+                                int8_t *q, float *s_a, qlin_stream_t stream);
+
+/*
+ * W8A8 GS128 linear:  y = bf16( s_a[m] * sum_g s_w[g,n] * P[g,m,n] ),
+ * P[g,m,n] = sum_{k = 128g}^{128g+127} q_a[m,k] * q_w[k,n]  (exact integers).
+ *
+ * Passages: "Qwen3.8-27B-GPTQ-INT8-W8A8-GS128-PTQR" card, "Quantization
+ * details" (true int8 x int8 compute at every decode and prefill GEMM shape,
+ * one weight scale per 128-wide K block); "Flint-DFlash2-GPTQ-INT8-PTQR"
+ * card, parameter table and the "AITER W8A8 INT8 GEMMs at every M" contract.
+ *
+ * Each group's partial P is computed exactly; groups are rescaled in fp32 by
+ * fma(P, s_w, acc) in ascending g, the result is multiplied once by s_a[m]
+ * and rounded to bf16 (nearest even).  When K is split across thread blocks
+ * the per-split fp32 partials are summed in ascending split order, so the
+ * result is deterministic for a given (M, N, K) and device.
+ *
+ *   q_a      int8  [M, K]          quantized activations (qlin_act_quant_i8)
+ *   s_a      fp32  [M]             activation scales
+ *   qweight  int32 [K/4, N]        GPTQ words: byte i of word (kk, n) holds
+ *                                  q_w[4kk+i, n] + 128, byte 0 least significant
+ *   scales   fp16  [K/128, N]      weight group scales s_w
+ *   y        bf16  [M, N]          output
+ *   workspace / workspace_bytes    at least qlin_workspace_bytes(M, N, K) bytes
+ *            of device memory, ZEROED BEFORE ITS FIRST USE.  It holds split-K
+ *            partials and arrival counters; the kernels return the counters to
+ *            zero, so the buffer can be reused by later calls that are ordered
+ *            on one stream.  Calls that share a workspace must not overlap.
+ *            After a device error (QLIN_ERR_DEVICE_TIMEOUT) zero it again.
+ */
+qlin_status_t qlin_gemm_w8a8_gs128(const int8_t *q_a, const float *s_a,
+                                   const int32_t *qweight, const uint16_t *scales,
+                                   int64_t M, int64_t N, int64_t K, uint16_t *y,
+                                   void *workspace, size_t workspace_bytes,
+                                   qlin_stream_t stream);
+
+/*
+ * W4A16 g128 symmetric weight-only linear:
+ *   w[k,n] = bf16( q_w[k,n] * s[k/128, n] ),   y = bf16( sum_k x[m,k] * w[k,n] )
+ * accumulated in fp32.
+ *
+ * Passages: "Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card, property table
+ * (4-bit weights, BF16 activations, group_size=128, symmetric; INT32-packed)
+ * and the apply_dense_kv_fix format table (W4A16 GPTQ: unpack_from_int32 +
+ * group scales).
+ *
+ *   x        bf16  [M, K]          activations
+ *   qweight  int32 [K/8, N]        nibble i (bits 4i..4i+3) of word (kk, n)
+ *                                  holds q_w[8kk+i, n] + 8
+ *   scales   bf16  [K/128, N]      group scales
+ *   y        bf16  [M, N]          output
+ *   workspace / workspace_bytes    as for qlin_gemm_w8a8_gs128
+ */
+qlin_status_t qlin_gemm_w4a16_g128(const uint16_t *x, const int32_t *qweight,
+                                   const uint16_t *scales, int64_t M, int64_t N,
+                                   int64_t K, uint16_t *y, void *workspace,
+                                   size_t workspace_bytes, qlin_stream_t stream);
+
+/*
+ * GPTQ packer (offline step; not on the timed path).
+ *
+ * Passages: "Flint-DFlash2-GPTQ-INT8-PTQR" card, parameter table (GPTQ
+ * qweight/qzeros/scales, INT8, symmetric, no g_idx);
+ * "Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card (INT32-packed 4-bit weights).
+ *
+ *   q        int8  [K, N]          weights, in [-2^(bits-1), 2^(bits-1) - 1]
+ *   bits     8 or 4
+ *   qweight  int32 [K*bits/32, N]  output: field i of word (kk, n) holds
+ *                                  q[(32/bits)*kk + i, n] + 2^(bits-1),
+ *                                  field 0 least significant
+ *   qzeros   int32 [K/128, N*bits/32] output or NULL; every field = 2^(bits-1)
+ *                                  (needs N*bits % 32 == 0 when not NULL)
+ * A value outside the range is packed masked and flags QLIN_ERR_VALUE_RANGE
+ * in the device error word.
+ */
+qlin_status_t qlin_pack_gptq(const int8_t *q, int64_t K, int64_t N, int bits,
+                             int32_t *qweight, int32_t *qzeros, qlin_stream_t stream);
+
+/*
+ * Bytes of workspace the two GEMMs need for (M, N, K) on the current device
+ * (split-K partials plus one counter per output tile).  Returns 0 for shapes
+ * the GEMMs reject.
+ */
+size_t qlin_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Test hook: the exact per-group integer partials of the W8A8 path,
+ * P[g, m, n] (int32 [K/128, M, N]), produced by the same tensor-core pipeline
+ * as qlin_gemm_w8a8_gs128 (exactly-converted int8 operands, fp32 TMEM
+ * accumulation of one 128-wide group), read back without rescaling.
+ * Meant for small shapes.  workspace as for the GEMM.
+ */
+qlin_status_t qlin_debug_group_partials_i8(const int8_t *q_a, const int32_t *qweight,
+                                           int64_t M, int64_t N, int64_t K,
+                                           int32_t *P, void *workspace,
+                                           size_t workspace_bytes, qlin_stream_t stream);
+
+/*
+ * Test hook: launches one block whose thread waits on a barrier that nothing
+ * completes, with a wait limit of limit_ns nanoseconds (1e3 .. 1e10).  The
+ * wait runs out, the kernel records QLIN_ERR_DEVICE_TIMEOUT in the device
+ * error word and returns normally; the CUDA context stays usable.
+ */
+qlin_status_t qlin_debug_wait_timeout(int64_t limit_ns, qlin_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device-wide error word of
+ * the current device.  Returns QLIN_OK, QLIN_ERR_DEVICE_TIMEOUT,
+ * QLIN_ERR_VALUE_RANGE, or QLIN_ERR_CUDA if the synchronization failed.
+ */
+qlin_status_t qlin_device_status(qlin_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *qlin_status_string(qlin_status_t status);
+
+/* Library ABI version (major * 100 + minor). */
+int qlin_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLIN_H */

@@ -1,0 +1,112 @@
+"""Full-size workloads through the C ABI, checked against the oracle on
+sampled columns (all rows, or sampled rows at M = 8192).  Shapes: the drafter
+layer's seven projections and the fc projection (hidden 5120, intermediate
+17408, 32 query / 8 key-value heads of 128, fc 25600 -> 5120), the 5120 ->
+248320 vocabulary head, at the decode, prefill and verification token counts
+of the serving recipes.  Inputs are synthetic (seeded), drawn as the
+workload recipe in the design notes states."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import compare_linear, from_dev_bits, to_dev, to_dev_bits
+from w4a16_linear_layers_gb300 import qlin, synth
+from w4a16_linear_layers_gb300 import build as qbuild
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    qbuild.build()
+    qlin.load()
+    oracle.build()
+    yield
+    assert qlin.device_status() == qlin.QLIN_OK
+
+
+def sample_cols(N, seed, blocks=2):
+    """All columns for N <= 1024; else `blocks` random 128-wide blocks plus the
+    last 128 columns (the tail tile)."""
+    if N <= 1024:
+        return np.arange(N)
+    nb = N // 128
+    pick = synth.choice_without_replacement(seed, f"cols/{N}", nb - 1, blocks)
+    cols = [np.arange(b * 128, b * 128 + 128) for b in pick]
+    cols.append(np.arange(N - 128, N))
+    return np.concatenate(cols)
+
+
+def sample_rows(M, seed, limit=96):
+    if M <= limit:
+        return np.arange(M)
+    rows = synth.choice_without_replacement(seed, f"rows/{M}", M - 2, limit - 2)
+    return np.concatenate([[0], rows + 1, [M - 1]])
+
+
+def run_w8a8(name, M, K, N, kind, seed=0):
+    xb = synth.activations(seed, synth.shared_input_name(name) + f"/M{M}", M, K, kind)
+    qwt, swb = synth.w8a8_weights(seed, name, K, N)
+    qw, _, _ = oracle.pack_gptq(qwt, 8)
+    del qwt
+    x_d = to_dev_bits(xb, torch.bfloat16)
+    qa_d, sa_d = qlin.act_quant_i8(x_d)
+    y_d = qlin.gemm_w8a8_gs128(qa_d, sa_d, to_dev(qw), to_dev_bits(swb, torch.float16))
+    torch.cuda.synchronize()
+    qa, sa = oracle.act_quant_i8(xb)
+    assert np.array_equal(qa_d.cpu().numpy(), qa) and np.array_equal(sa_d.cpu().numpy(), sa)
+    rows, cols = sample_rows(M, seed), sample_cols(N, seed)
+    y = from_dev_bits(y_d)[np.ix_(rows, cols)]
+    ref = oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K, rows, cols)
+    return compare_linear(y, ref, f"{name} M={M}")
+
+
+def run_w4a16(name, M, K, N, seed=0):
+    xb = synth.activations(seed, synth.shared_input_name(name) + f"/w4/M{M}", M, K, "normal")
+    qwt, sb = synth.w4a16_weights(seed, name + "/w4", K, N)
+    qw, _, _ = oracle.pack_gptq(qwt, 4)
+    del qwt
+    y_d = qlin.gemm_w4a16_g128(to_dev_bits(xb, torch.bfloat16), to_dev(qw),
+                               to_dev_bits(sb, torch.bfloat16))
+    torch.cuda.synchronize()
+    rows, cols = sample_rows(M, seed), sample_cols(N, seed)
+    y = from_dev_bits(y_d)[np.ix_(rows, cols)]
+    ref = oracle.gemm_w4a16_g128(xb, qw, sb, K, rows, cols)
+    return compare_linear(y, ref, f"{name} w4a16 M={M}")
+
+
+def test_single_w8a8_linear_all_outputs():
+    """5120 -> 1024 at M = 8, every output checked."""
+    st = run_w8a8("single", 8, 5120, 1024, "outliers")
+    assert st["n"] == 8 * 1024
+
+
+@pytest.mark.parametrize("M", [8, 64, 96])
+def test_drafter_layer_w8a8(M):
+    for name, K, N, kind in synth.DRAFTER_LAYER:
+        run_w8a8(f"layers.0.{name}", M, K, N, kind)
+
+
+def test_fc_projection_w8a8():
+    name, K, N, kind = synth.FC
+    run_w8a8(name, 96, K, N, kind)
+
+
+@pytest.mark.parametrize("M", [8, 64])
+def test_drafter_w4a16(M):
+    for name, K, N, _ in synth.DRAFTER_LAYER + (synth.FC,):
+        run_w4a16(name, M, K, N)
+
+
+@pytest.mark.parametrize("M", [128, 512, 2048, 8192])
+def test_prefill_mlp_w8a8(M):
+    run_w8a8("layers.0.gate_proj", M, 5120, 17408, "outliers")
+    run_w8a8("layers.0.down_proj", M, 17408, 5120, "silu_mul")
+
+
+@pytest.mark.parametrize("M", [8, 96])
+def test_vocab_head_w8a8(M):
+    run_w8a8("lm_head", M, 5120, 248320, "outliers")

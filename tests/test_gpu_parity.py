@@ -1,0 +1,256 @@
+"""CUDA path vs the CPU oracle, through the C ABI (the ctypes binding).
+
+Integer stages (quantized activations, activation scales, packed words, the
+per-group integer partials) must be bit-exact; bf16 outputs must meet the
+tolerance in tests/helpers.py.  Sizes span several tiles and a ragged tail;
+the full-size workloads are checked on sampled columns (every row, since rows
+are independent)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import compare_linear, from_dev_bits, to_dev, to_dev_bits
+from w4a16_linear_layers_gb300 import qlin, synth
+from w4a16_linear_layers_gb300 import build as qbuild
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    qbuild.build()
+    qlin.load()
+    oracle.build()
+    assert qlin.device_status() == qlin.QLIN_OK
+    yield
+    assert qlin.device_status() == qlin.QLIN_OK
+
+
+def _act_quant_gpu(xb):
+    q, s = qlin.act_quant_i8(to_dev_bits(xb, torch.bfloat16))
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().numpy()
+
+
+# ------------------------------------------------------------- act-quant
+
+@pytest.mark.parametrize("M,K,kind", [
+    (1, 128, "normal"), (3, 5120, "outliers"), (8, 5120, "outliers"), (17, 4096, "normal2"),
+    (96, 17408, "silu_mul"), (5, 25600, "normal2"), (4, 33024, "outliers"), (130, 640, "normal"),
+])
+def test_act_quant_bit_exact(M, K, kind):
+    xb = synth.activations(1, f"gpu/aq/{M}/{K}", M, K, kind)
+    if M > 2:
+        xb[0, : min(K, 256)] = 0         # a partly-zero row
+        xb[1, :] = 0                     # an all-zero row
+    q, s = _act_quant_gpu(xb)
+    oq, os_ = oracle.act_quant_i8(xb)
+    assert np.array_equal(s.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(q, oq)
+
+
+def test_act_quant_ties_and_divide_cases():
+    rows = [
+        [127, 2.5, -3.5, 0.5, 1.5, -0.5, -1.5, 126.5],
+        [254, 1, 3, -1, 5, -7, -254, 100],
+        [0] * 8,
+    ]
+    x = np.zeros((3, 128), np.float32)
+    for i, r in enumerate(rows):
+        x[i, : len(r)] = r
+    xb = synth.bf16_bits(x)
+    q, s = _act_quant_gpu(xb)
+    oq, os_ = oracle.act_quant_i8(xb)
+    assert np.array_equal(q, oq) and np.array_equal(s, os_)
+    assert q[0, :8].tolist() == [127, 2, -4, 0, 2, 0, -2, 126]
+    # many random rows: elements near .5 boundaries included by volume
+    xb = synth.activations(77, "gpu/aq/many", 512, 1024, "normal")
+    q, s = _act_quant_gpu(xb)
+    oq, os_ = oracle.act_quant_i8(xb)
+    assert np.array_equal(q, oq) and np.array_equal(s, os_)
+
+
+# ------------------------------------------------------------------ pack
+
+@pytest.mark.parametrize("bits,K,N", [(8, 256, 40), (8, 5120, 1024), (4, 384, 72), (4, 5120, 1000)])
+def test_pack_bit_exact(bits, K, N):
+    lo, hi = (-128, 127) if bits == 8 else (-8, 7)
+    q = synth.randint(2, f"gpu/pack/{bits}/{K}/{N}", (K, N), lo, hi)
+    qw, qz = qlin.pack_gptq(to_dev(q), bits, with_qzeros=(N * bits) % 32 == 0)
+    oqw, oqz, bad = oracle.pack_gptq(q, bits)
+    assert bad == 0
+    assert np.array_equal(qw.cpu().numpy(), oqw)
+    if qz is not None:
+        assert np.array_equal(qz.cpu().numpy(), oqz)
+    assert qlin.device_status() == qlin.QLIN_OK
+
+
+def test_pack_flags_out_of_range():
+    q = np.zeros((128, 8), np.int8)
+    q[5, 3] = 9
+    qlin.pack_gptq(to_dev(q), 4)
+    assert qlin.device_status() == qlin.QLIN_ERR_VALUE_RANGE
+    assert qlin.device_status() == qlin.QLIN_OK      # the error word was cleared
+
+
+# ---------------------------------------------------- W8A8 group partials
+
+def _w8a8_inputs(seed, name, M, K, N, kind="outliers"):
+    xb = synth.activations(seed, name + "/x", M, K, kind)
+    qa, sa = oracle.act_quant_i8(xb)
+    qwt, swb = synth.w8a8_weights(seed, name + "/w", K, N)
+    qw, _, _ = oracle.pack_gptq(qwt, 8)
+    return xb, qa, sa, qwt, qw, swb
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 128, 128), (8, 640, 256), (17, 384, 200), (96, 256, 384),
+                                   (130, 256, 136)])
+def test_group_partials_bit_exact(M, K, N):
+    _, qa, _, _, qw, _ = _w8a8_inputs(3, f"gpu/gp/{M}/{K}/{N}", M, K, N)
+    P = qlin.debug_group_partials_i8(to_dev(qa), to_dev(qw))
+    torch.cuda.synchronize()
+    assert np.array_equal(P.cpu().numpy(), oracle.group_partials_i8(qa, qw, K))
+
+
+def test_group_partials_extreme_magnitudes():
+    """All +-127 operands: |P| = 128*127^2 = 2,064,512, the largest partial;
+    fp16 operands with fp32 tensor-memory accumulation must stay exact."""
+    M, K, N = 64, 512, 256
+    sign_a = synth.randint(4, "gpu/gp/xa", (M, K), 0, 1) * 2 - 1
+    sign_w = synth.randint(4, "gpu/gp/xw", (K, N), 0, 1) * 2 - 1
+    qa = (127 * sign_a).astype(np.int8)
+    qa[0] = 127
+    qwt = (127 * sign_w).astype(np.int8)
+    qwt[:, 0] = 127
+    qw, _, _ = oracle.pack_gptq(qwt, 8)
+    P = qlin.debug_group_partials_i8(to_dev(qa), to_dev(qw)).cpu().numpy()
+    ref = oracle.group_partials_i8(qa, qw, K)
+    assert ref[:, 0, 0].tolist() == [128 * 127 * 127] * (K // 128)
+    assert np.array_equal(P, ref)
+
+
+# -------------------------------------------------------------- W8A8 GEMM
+
+def _gemm_w8a8_gpu(qa, sa, qw, swb, workspace=None):
+    y = qlin.gemm_w8a8_gs128(to_dev(qa), to_dev(sa), to_dev(qw), to_dev_bits(swb, torch.float16),
+                             workspace=workspace)
+    torch.cuda.synchronize()
+    return from_dev_bits(y)
+
+
+@pytest.mark.parametrize("M,K,N", [
+    (1, 128, 128), (3, 256, 200), (8, 5120, 1024), (16, 1280, 384), (17, 640, 256),
+    (64, 4096, 512), (96, 2560, 768), (100, 384, 136), (128, 512, 256), (257, 768, 264),
+])
+def test_w8a8_matches_oracle(M, K, N):
+    _, qa, sa, _, qw, swb = _w8a8_inputs(5, f"gpu/w8/{M}/{K}/{N}", M, K, N)
+    y = _gemm_w8a8_gpu(qa, sa, qw, swb)
+    compare_linear(y, oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K), f"w8a8 {M}x{K}x{N}")
+
+
+def test_w8a8_identity_probe():
+    """Feeding I_K recovers the effective weight q*s (single nonzero group per
+    row, so every split of K gives the oracle's exact fp32 chain)."""
+    K, N = 384, 256
+    xb = synth.bf16_bits(np.eye(K, dtype=np.float32))
+    qa, sa = oracle.act_quant_i8(xb)
+    qwt, swb = synth.w8a8_weights(6, "gpu/w8/probe", K, N)
+    qw, _, _ = oracle.pack_gptq(qwt, 8)
+    y = _gemm_w8a8_gpu(qa, sa, qw, swb)
+    ref = oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K)
+    assert np.array_equal(y, ref["y_bf16"])
+
+
+def test_w8a8_deterministic_and_workspace_reuse():
+    M, K, N = 8, 5120, 1024
+    _, qa, sa, _, qw, swb = _w8a8_inputs(7, "gpu/w8/det", M, K, N)
+    ws = qlin.Workspace()
+    y1 = _gemm_w8a8_gpu(qa, sa, qw, swb, ws)
+    y2 = _gemm_w8a8_gpu(qa, sa, qw, swb, ws)
+    assert np.array_equal(y1, y2)
+    plan_bytes = qlin.workspace_bytes(M, N, K)
+    counters = ws.buf[: min(plan_bytes, 4096)].view(torch.int32).cpu().numpy()
+    assert not counters[: (N // 128)].any(), "split-K counters must return to zero"
+
+
+# ------------------------------------------------------------- W4A16 GEMM
+
+def _w4a16_inputs(seed, name, M, K, N, kind="normal"):
+    xb = synth.activations(seed, name + "/x", M, K, kind)
+    qwt, sb = synth.w4a16_weights(seed, name + "/w", K, N)
+    qw, _, _ = oracle.pack_gptq(qwt, 4)
+    return xb, qwt, qw, sb
+
+
+def _gemm_w4a16_gpu(xb, qw, sb, workspace=None):
+    y = qlin.gemm_w4a16_g128(to_dev_bits(xb, torch.bfloat16), to_dev(qw),
+                             to_dev_bits(sb, torch.bfloat16), workspace=workspace)
+    torch.cuda.synchronize()
+    return from_dev_bits(y)
+
+
+@pytest.mark.parametrize("M,K,N", [
+    (1, 128, 128), (3, 256, 200), (8, 5120, 1024), (17, 640, 256), (64, 4096, 512),
+    (96, 1280, 384), (130, 512, 264),
+])
+def test_w4a16_matches_oracle(M, K, N):
+    xb, _, qw, sb = _w4a16_inputs(9, f"gpu/w4/{M}/{K}/{N}", M, K, N)
+    y = _gemm_w4a16_gpu(xb, qw, sb)
+    compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), f"w4a16 {M}x{K}x{N}")
+
+
+def test_w4a16_identity_probe_bit_exact():
+    K, N = 256, 384
+    _, qwt, qw, sb = _w4a16_inputs(10, "gpu/w4/probe", 1, K, N)
+    xb = synth.bf16_bits(np.eye(K, dtype=np.float32))
+    y = _gemm_w4a16_gpu(xb, qw, sb)
+    assert np.array_equal(y, oracle.dequant_w4a16(qw, sb, K, N))
+
+
+def test_w4a16_full_nibble_range():
+    """q = -8 (nibble 0) decodes to -8 as well."""
+    M, K, N = 8, 256, 128
+    xb = synth.activations(11, "gpu/w4/nib/x", M, K, "normal")
+    qwt = synth.randint(11, "gpu/w4/nib/w", (K, N), -8, 7)
+    qw, _, _ = oracle.pack_gptq(qwt, 4)
+    sb = synth.bf16_bits(synth.log_uniform(11, "gpu/w4/nib/s", (K // 128, N), 1e-3, 3e-2))
+    y = _gemm_w4a16_gpu(xb, qw, sb)
+    compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), "w4a16 nibble range")
+
+
+# ------------------------------------------------------------ host checks
+
+def test_argument_errors_return_status():
+    lib = qlin.load()
+    x = torch.zeros((8, 256), dtype=torch.int8, device="cuda")
+    s = torch.zeros(8, dtype=torch.float32, device="cuda")
+    qw = torch.zeros((64, 128), dtype=torch.int32, device="cuda")
+    sc = torch.zeros((2, 128), dtype=torch.float16, device="cuda")
+    y = torch.zeros((8, 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(qlin.workspace_bytes(8, 128, 256), dtype=torch.uint8, device="cuda")
+    P = lambda t: t.data_ptr()
+    st = torch.cuda.current_stream().cuda_stream
+    f = lib.qlin_gemm_w8a8_gs128
+    assert f(None, P(s), P(qw), P(sc), 8, 128, 256, P(y), P(ws), ws.numel(), st) == qlin.QLIN_ERR_NULL
+    assert f(P(x), P(s), P(qw), P(sc), 8, 128, 200, P(y), P(ws), ws.numel(), st) == qlin.QLIN_ERR_SHAPE
+    assert f(P(x), P(s), P(qw), P(sc), 8, 124, 256, P(y), P(ws), ws.numel(), st) == qlin.QLIN_ERR_SHAPE
+    assert f(P(x) + 1, P(s), P(qw), P(sc), 8, 128, 256, P(y), P(ws), ws.numel(), st) == qlin.QLIN_ERR_ALIGN
+    assert f(P(x), P(s), P(qw), P(sc), 8, 128, 256, P(y), P(ws), 16, st) == qlin.QLIN_ERR_WORKSPACE
+    assert f(P(x), P(s), P(qw), P(sc), 0, 128, 256, P(y), P(ws), ws.numel(), st) == qlin.QLIN_OK
+    assert lib.qlin_pack_gptq(P(x), 256, 8, 5, P(qw), None, st) == qlin.QLIN_ERR_BITS
+    assert lib.qlin_act_quant_i8(P(y), 8, 100, P(x), P(s), st) == qlin.QLIN_ERR_SHAPE
+    assert qlin.device_status() == qlin.QLIN_OK
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    qlin.debug_wait_timeout(2_000_000)      # 2 ms limit on a barrier nothing completes
+    assert qlin.device_status() == qlin.QLIN_ERR_DEVICE_TIMEOUT
+    assert qlin.device_status() == qlin.QLIN_OK
+    # the context still works
+    xb = synth.activations(1, "gpu/after-timeout", 4, 256, "normal")
+    q, s = _act_quant_gpu(xb)
+    oq, _ = oracle.act_quant_i8(xb)
+    assert np.array_equal(q, oq)

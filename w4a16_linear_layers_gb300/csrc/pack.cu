@@ -1,0 +1,89 @@
+// pack.cu -- GPTQ packer (offline step) and the bounded-wait test kernel.
+//
+// Packing follows the GPTQ format of the "Flint-DFlash2-GPTQ-INT8-PTQR" card
+// (qweight/qzeros, symmetric, INT8) and the INT32-packed 4-bit weights of the
+// "Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card: field i of word (kk, n)
+// holds q[(32/bits)*kk + i, n] + 2^(bits-1), field 0 least significant.
+#include "qlin_device.cuh"
+#include "qlin_internal.h"
+
+namespace qlin {
+namespace {
+
+template <int kBits>
+__global__ void pack_kernel(const int8_t* __restrict__ q, int64_t N, int64_t words,
+                            int32_t* __restrict__ qweight, int* err) {
+  constexpr int kPer = 32 / kBits;
+  constexpr int kZero = 1 << (kBits - 1);
+  constexpr uint32_t kMask = (1u << kBits) - 1u;
+  bool bad = false;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < words;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t kk = i / N;
+    const int64_t n = i - kk * N;
+    uint32_t word = 0;
+#pragma unroll
+    for (int f = 0; f < kPer; ++f) {
+      const int v = static_cast<int>(q[(kk * kPer + f) * N + n]) + kZero;
+      bad |= (v < 0) || (v > static_cast<int>(kMask));
+      word |= (static_cast<uint32_t>(v) & kMask) << (kBits * f);
+    }
+    qweight[i] = static_cast<int32_t>(word);
+  }
+  if (bad) report_error(err, kDevValueRange, 0);
+}
+
+__global__ void fill_kernel(int32_t* __restrict__ dst, int64_t count, uint32_t value) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = static_cast<int32_t>(value);
+}
+
+// One thread waits on a barrier that nothing completes; the bounded wait runs
+// out, records kDevTimeout and the kernel returns normally.
+__global__ void wait_timeout_kernel(int64_t limit_ns, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtx ctx{err, &abort_flag, static_cast<uint64_t>(limit_ns)};
+    (void)mbar_wait(smem_u32(&bar), 0, ctx, /*where=*/9999);
+  }
+}
+
+unsigned grid_for(int64_t n, int threads) {
+  int64_t blocks = (n + threads - 1) / threads;
+  if (blocks > 65535LL * 16) blocks = 65535LL * 16;
+  if (blocks < 1) blocks = 1;
+  return static_cast<unsigned>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const int8_t* q, int64_t K, int64_t N, int bits, int32_t* qweight,
+                        int32_t* qzeros, int* err, cudaStream_t stream) {
+  const int per = 32 / bits;
+  const int64_t words = (K / per) * N;
+  if (bits == 8)
+    pack_kernel<8><<<grid_for(words, 256), 256, 0, stream>>>(q, N, words, qweight, err);
+  else
+    pack_kernel<4><<<grid_for(words, 256), 256, 0, stream>>>(q, N, words, qweight, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || qzeros == nullptr) return e;
+  const int64_t zwords = (K / kGroup) * (N / per);
+  const uint32_t zword = bits == 8 ? 0x80808080u : 0x88888888u;
+  fill_kernel<<<grid_for(zwords, 256), 256, 0, stream>>>(qzeros, zwords, zword);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout(int64_t limit_ns, int* err, cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+  return cudaGetLastError();
+}
+
+}  // namespace qlin

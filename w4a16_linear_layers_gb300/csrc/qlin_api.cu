@@ -1,0 +1,210 @@
+// qlin_api.cu -- the extern "C" entry points of libqlin (include/qlin.h):
+// argument checks, per-device state (SM count, architecture, the device error
+// word) and dispatch to the launchers.  No call allocates device memory.
+#include <mutex>
+
+#include "../../include/qlin.h"
+#include "qlin_device.cuh"
+#include "qlin_internal.h"
+
+namespace qlin {
+
+// Device-wide error word: [0] = code, [1] = where, [2] = block, [3] = spare.
+__device__ int g_error_word[4];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::once_flag g_device_once[kMaxDevices];
+
+void init_device(int dev) {
+  DeviceInfo& d = g_devices[dev];
+  d.device = dev;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  d.supported = (major == 10 && minor == 3);
+  if (!d.supported) return;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) {
+    cudaGetLastError();
+    d.supported = false;
+    return;
+  }
+  d.err_word = static_cast<int*>(addr);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kMaxDim = 2147483647LL;
+
+qlin_status_t check_gemm_shape(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || M > kMaxDim || N < 8 || N > kMaxDim || (N % 8) != 0 || K < kGroup ||
+      K > kMaxDim || (K % kGroup) != 0)
+    return QLIN_ERR_SHAPE;
+  return QLIN_OK;
+}
+
+}  // namespace
+
+const DeviceInfo* current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::call_once(g_device_once[dev], init_device, dev);
+  return &g_devices[dev];
+}
+
+}  // namespace qlin
+
+using namespace qlin;
+
+namespace {
+
+qlin_status_t device_or_error(const DeviceInfo** out) {
+  const DeviceInfo* d = current_device();
+  if (d == nullptr || !d->supported) return QLIN_ERR_DEVICE;
+  *out = d;
+  return QLIN_OK;
+}
+
+qlin_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA; }
+
+qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const int32_t* qweight,
+                       const uint16_t* scales, void* out, int64_t M, int64_t N, int64_t K,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (act == nullptr || qweight == nullptr || out == nullptr ||
+      (mode != GemmMode::kW8A8Partials && scales == nullptr) ||
+      (mode == GemmMode::kW8A8 && s_a == nullptr))
+    return QLIN_ERR_NULL;
+  qlin_status_t st = check_gemm_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  if (!aligned16(act) || !aligned16(qweight) || !aligned16(out) ||
+      (scales && !aligned16(scales)) || (s_a && !aligned16(s_a)) ||
+      (workspace && !aligned16(workspace)))
+    return QLIN_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  if (M == 0) return QLIN_OK;
+  const GemmPlan plan = plan_gemm(M, N, K, d->sm_count);
+  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return QLIN_ERR_WORKSPACE;
+  GemmArgs a{mode, act, s_a, qweight, scales, out, M, N, K, workspace, workspace_bytes};
+  return from_cuda(launch_gemm(a, plan, d->err_word, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+qlin_status_t qlin_act_quant_i8(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s_a,
+                                qlin_stream_t stream) {
+  if (x == nullptr || q == nullptr || s_a == nullptr) return QLIN_ERR_NULL;
+  if (M < 0 || M > kMaxDim || K < kGroup || K > kMaxDim || (K % kGroup) != 0)
+    return QLIN_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s_a)) return QLIN_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  qlin_status_t st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  if (M == 0) return QLIN_OK;
+  return from_cuda(launch_act_quant(x, M, K, q, s_a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_gemm_w8a8_gs128(const int8_t* q_a, const float* s_a, const int32_t* qweight,
+                                   const uint16_t* scales, int64_t M, int64_t N, int64_t K,
+                                   uint16_t* y, void* workspace, size_t workspace_bytes,
+                                   qlin_stream_t stream) {
+  return run_gemm(GemmMode::kW8A8, q_a, s_a, qweight, scales, y, M, N, K, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_gemm_w4a16_g128(const uint16_t* x, const int32_t* qweight,
+                                   const uint16_t* scales, int64_t M, int64_t N, int64_t K,
+                                   uint16_t* y, void* workspace, size_t workspace_bytes,
+                                   qlin_stream_t stream) {
+  return run_gemm(GemmMode::kW4A16, x, nullptr, qweight, scales, y, M, N, K, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_debug_group_partials_i8(const int8_t* q_a, const int32_t* qweight, int64_t M,
+                                           int64_t N, int64_t K, int32_t* P, void* workspace,
+                                           size_t workspace_bytes, qlin_stream_t stream) {
+  return run_gemm(GemmMode::kW8A8Partials, q_a, nullptr, qweight, nullptr, P, M, N, K, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_pack_gptq(const int8_t* q, int64_t K, int64_t N, int bits, int32_t* qweight,
+                             int32_t* qzeros, qlin_stream_t stream) {
+  if (q == nullptr || qweight == nullptr) return QLIN_ERR_NULL;
+  if (bits != 4 && bits != 8) return QLIN_ERR_BITS;
+  if (K < kGroup || K > kMaxDim || (K % kGroup) != 0 || N < 1 || N > kMaxDim)
+    return QLIN_ERR_SHAPE;
+  if (qzeros != nullptr && (N * bits) % 32 != 0) return QLIN_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(qweight) || (qzeros && !aligned16(qzeros))) return QLIN_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  qlin_status_t st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  return from_cuda(launch_pack(q, K, N, bits, qweight, qzeros, d->err_word,
+                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t qlin_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (check_gemm_shape(M, N, K) != QLIN_OK || M == 0) return 0;
+  const DeviceInfo* d = current_device();
+  if (d == nullptr || !d->supported) return 0;
+  return plan_gemm(M, N, K, d->sm_count).workspace_bytes;
+}
+
+qlin_status_t qlin_debug_wait_timeout(int64_t limit_ns, qlin_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 10000000000LL) return QLIN_ERR_SHAPE;
+  const DeviceInfo* d = nullptr;
+  qlin_status_t st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  return from_cuda(launch_wait_timeout(limit_ns, d->err_word, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_device_status(qlin_stream_t stream) {
+  const DeviceInfo* d = nullptr;
+  qlin_status_t st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return QLIN_ERR_CUDA;
+  int word[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(word, d->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return QLIN_ERR_CUDA;
+  if (word[0] != 0) {
+    const int zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(d->err_word, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return QLIN_ERR_CUDA;
+  }
+  if (word[0] == kDevTimeout) return QLIN_ERR_DEVICE_TIMEOUT;
+  if (word[0] == kDevValueRange) return QLIN_ERR_VALUE_RANGE;
+  return QLIN_OK;
+}
+
+const char* qlin_status_string(qlin_status_t status) {
+  switch (status) {
+    case QLIN_OK: return "ok";
+    case QLIN_ERR_NULL: return "a required pointer is NULL";
+    case QLIN_ERR_SHAPE: return "invalid shape (K must be a positive multiple of 128, N a positive multiple of 8)";
+    case QLIN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case QLIN_ERR_WORKSPACE: return "workspace is NULL or smaller than qlin_workspace_bytes()";
+    case QLIN_ERR_BITS: return "bits must be 4 or 8";
+    case QLIN_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    case QLIN_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case QLIN_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case QLIN_ERR_VALUE_RANGE: return "the packer met a value outside the bit width";
+    default: return "unknown status";
+  }
+}
+
+int qlin_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// qlin_internal.h -- host-side declarations shared by the translation units
+// of libqlin (launchers called from the C ABI in qlin_api.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qlin {
+
+// Per-device facts cached by the API layer.
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  bool supported = false;  // sm_103
+  int* err_word = nullptr; // device address of the error word
+};
+
+// Returns the cached info of the current device (nullptr if no device).
+const DeviceInfo* current_device();
+
+cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s,
+                             cudaStream_t stream);
+
+cudaError_t launch_pack(const int8_t* q, int64_t K, int64_t N, int bits, int32_t* qweight,
+                        int32_t* qzeros, int* err, cudaStream_t stream);
+
+cudaError_t launch_wait_timeout(int64_t limit_ns, int* err, cudaStream_t stream);
+
+// GEMM problem description passed from the API to the launcher.
+enum class GemmMode : int { kW8A8 = 0, kW8A8Partials = 1, kW4A16 = 2 };
+
+struct GemmArgs {
+  GemmMode mode;
+  const void* act;        // int8 q_a [M,K] (W8A8) or bf16 x [M,K] (W4A16)
+  const float* s_a;       // W8A8 only
+  const int32_t* qweight; // [K/4,N] or [K/8,N]
+  const uint16_t* scales; // fp16 (W8A8) or bf16 (W4A16) [K/128,N]
+  void* out;              // bf16 y [M,N] or int32 P [K/128,M,N]
+  int64_t M, N, K;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+// Tiling plan for one GEMM call.
+struct GemmPlan {
+  int T;           // token tile (MMA N): 16, 32, 64, 96 or 128
+  int64_t F;       // feature tiles of 128
+  int64_t TT;      // token tiles
+  int64_t G;       // groups of 128 along K
+  int64_t steps;   // TT * F * G
+  int64_t ctas;    // grid size
+  size_t counter_bytes;
+  size_t workspace_bytes;
+};
+
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count);
+
+cudaError_t launch_gemm(const GemmArgs& a, const GemmPlan& p, int* err, cudaStream_t stream);
+
+}  // namespace qlin

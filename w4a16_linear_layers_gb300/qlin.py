@@ -1,0 +1,263 @@
+"""Python binding of libqlin (ctypes).  Argument marshalling only: every step
+of the computation runs in the library's CUDA kernels; PyTorch supplies device
+memory and the current stream.
+
+Names follow the C ABI (include/qlin.h) without the ``qlin_`` prefix.  Tensors
+must be CUDA tensors, contiguous, of the dtypes listed per call; outputs are
+allocated with ``torch.empty`` when not given.  A non-zero status raises
+``QlinError``.  If the shared library has not been built the first call raises
+``QlinError`` -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+QLIN_OK = 0
+QLIN_ERR_NULL = -1
+QLIN_ERR_SHAPE = -2
+QLIN_ERR_ALIGN = -3
+QLIN_ERR_WORKSPACE = -4
+QLIN_ERR_BITS = -5
+QLIN_ERR_DEVICE = -6
+QLIN_ERR_CUDA = -10
+QLIN_ERR_DEVICE_TIMEOUT = -20
+QLIN_ERR_VALUE_RANGE = -21
+
+EXPORTS = (
+    "qlin_act_quant_i8",
+    "qlin_gemm_w8a8_gs128",
+    "qlin_gemm_w4a16_g128",
+    "qlin_pack_gptq",
+    "qlin_workspace_bytes",
+    "qlin_debug_group_partials_i8",
+    "qlin_debug_wait_timeout",
+    "qlin_device_status",
+    "qlin_status_string",
+    "qlin_version",
+)
+
+
+class QlinError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"qlin status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load libqlin.so (built in-tree by ``w4a16_linear_layers_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise QlinError(QLIN_ERR_CUDA, f"{path} is not built; run "
+                            "`python -m w4a16_linear_layers_gb300.build` (or __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        sig = {
+            "qlin_act_quant_i8": ([P, I64, I64, P, P, P], I),
+            "qlin_gemm_w8a8_gs128": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_gemm_w4a16_g128": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_pack_gptq": ([P, I64, I64, I, P, P, P], I),
+            "qlin_workspace_bytes": ([I64, I64, I64], SZ),
+            "qlin_debug_group_partials_i8": ([P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_debug_wait_timeout": ([I64, P], I),
+            "qlin_device_status": ([P], I),
+            "qlin_status_string": ([I], ctypes.c_char_p),
+            "qlin_version": ([], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().qlin_status_string(int(status)).decode()
+
+
+def _check(status: int) -> None:
+    if status != QLIN_OK:
+        raise QlinError(status, status_string(status))
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(handle)
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ------------------------------------------------------------------- calls
+
+def act_quant_i8(x: torch.Tensor, q: torch.Tensor | None = None, s_a: torch.Tensor | None = None,
+                 stream=None):
+    """x bf16 [M,K] -> (q int8 [M,K], s_a fp32 [M])."""
+    _need(x, "x", torch.bfloat16, 2)
+    M, K = x.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if s_a is None:
+        s_a = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(q, "q", torch.int8, 2)
+    _need(s_a, "s_a", torch.float32, 1)
+    _check(load().qlin_act_quant_i8(_ptr(x), M, K, _ptr(q), _ptr(s_a), _stream_handle(stream)))
+    return q, s_a
+
+
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().qlin_workspace_bytes(int(M), int(N), int(K)))
+
+
+class Workspace:
+    """A zero-initialised device buffer for the GEMMs' split-K partials and
+    counters, grown on demand.  The kernels return the counters to zero, so one
+    Workspace serves any number of calls ordered on one stream."""
+
+    def __init__(self, device=None, nbytes: int = 0):
+        self.device = torch.device(device if device is not None else "cuda")
+        self.buf = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
+
+    def get(self, M: int, N: int, K: int) -> torch.Tensor:
+        need = workspace_bytes(M, N, K)
+        if need > self.buf.numel():
+            self.buf = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _workspace(ws, M, N, K, device):
+    if ws is None:
+        key = (device.index if device.index is not None else torch.cuda.current_device())
+        ws = _default_ws.get(key)
+        if ws is None:
+            ws = _default_ws[key] = Workspace(device)
+    if isinstance(ws, Workspace):
+        return ws.get(M, N, K)
+    return ws
+
+
+def gemm_w8a8_gs128(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
+                    scales: torch.Tensor, y: torch.Tensor | None = None, workspace=None,
+                    stream=None) -> torch.Tensor:
+    """q_a int8 [M,K], s_a fp32 [M], qweight int32 [K/4,N], scales fp16 [K/128,N]
+    -> y bf16 [M,N]."""
+    _need(q_a, "q_a", torch.int8, 2)
+    _need(s_a, "s_a", torch.float32, 1)
+    _need(qweight, "qweight", torch.int32, 2)
+    _need(scales, "scales", torch.float16, 2)
+    M, K = q_a.shape
+    N = qweight.shape[1]
+    if qweight.shape[0] * 4 != K or scales.shape != (K // 128, N) or s_a.shape[0] != M:
+        raise ValueError("inconsistent W8A8 shapes")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=q_a.device)
+    _need(y, "y", torch.bfloat16, 2)
+    ws = _workspace(workspace, M, N, K, q_a.device)
+    _check(load().qlin_gemm_w8a8_gs128(_ptr(q_a), _ptr(s_a), _ptr(qweight), _ptr(scales), M, N, K,
+                                       _ptr(y), _ptr(ws), ws.numel(), _stream_handle(stream)))
+    return y
+
+
+def gemm_w4a16_g128(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                    y: torch.Tensor | None = None, workspace=None, stream=None) -> torch.Tensor:
+    """x bf16 [M,K], qweight int32 [K/8,N], scales bf16 [K/128,N] -> y bf16 [M,N]."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(qweight, "qweight", torch.int32, 2)
+    _need(scales, "scales", torch.bfloat16, 2)
+    M, K = x.shape
+    N = qweight.shape[1]
+    if qweight.shape[0] * 8 != K or scales.shape != (K // 128, N):
+        raise ValueError("inconsistent W4A16 shapes")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", torch.bfloat16, 2)
+    ws = _workspace(workspace, M, N, K, x.device)
+    _check(load().qlin_gemm_w4a16_g128(_ptr(x), _ptr(qweight), _ptr(scales), M, N, K, _ptr(y),
+                                       _ptr(ws), ws.numel(), _stream_handle(stream)))
+    return y
+
+
+def pack_gptq(q: torch.Tensor, bits: int, qweight: torch.Tensor | None = None,
+              qzeros: torch.Tensor | None = None, with_qzeros: bool = True, stream=None):
+    """q int8 [K,N] -> (qweight int32 [K*bits/32,N], qzeros int32 [K/128,N*bits/32] or None)."""
+    _need(q, "q", torch.int8, 2)
+    K, N = q.shape
+    per = 32 // bits if bits in (4, 8) else 1
+    if qweight is None:
+        qweight = torch.empty((K // per, N), dtype=torch.int32, device=q.device)
+    if qzeros is None and with_qzeros:
+        qzeros = torch.empty((K // 128, N // per), dtype=torch.int32, device=q.device)
+    _need(qweight, "qweight", torch.int32, 2)
+    zp = ctypes.c_void_p(0)
+    if qzeros is not None:
+        _need(qzeros, "qzeros", torch.int32, 2)
+        zp = _ptr(qzeros)
+    _check(load().qlin_pack_gptq(_ptr(q), K, N, int(bits), _ptr(qweight), zp,
+                                 _stream_handle(stream)))
+    return qweight, qzeros
+
+
+def debug_group_partials_i8(q_a: torch.Tensor, qweight: torch.Tensor, P: torch.Tensor | None = None,
+                            workspace=None, stream=None) -> torch.Tensor:
+    """Exact per-group integer partials P int32 [K/128, M, N] of the W8A8 path."""
+    _need(q_a, "q_a", torch.int8, 2)
+    _need(qweight, "qweight", torch.int32, 2)
+    M, K = q_a.shape
+    N = qweight.shape[1]
+    if P is None:
+        P = torch.empty((K // 128, M, N), dtype=torch.int32, device=q_a.device)
+    _need(P, "P", torch.int32, 3)
+    ws = _workspace(workspace, M, N, K, q_a.device)
+    _check(load().qlin_debug_group_partials_i8(_ptr(q_a), _ptr(qweight), M, N, K, _ptr(P),
+                                               _ptr(ws), ws.numel(), _stream_handle(stream)))
+    return P
+
+
+def debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(load().qlin_debug_wait_timeout(int(limit_ns), _stream_handle(stream)))
+
+
+def device_status(stream=None) -> int:
+    """Synchronize the stream, read and clear the device error word; returns the status."""
+    return int(load().qlin_device_status(_stream_handle(stream)))
+
+
+def version() -> int:
+    return int(load().qlin_version())
