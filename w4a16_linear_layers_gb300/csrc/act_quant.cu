@@ -58,6 +58,11 @@ __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint16_t* _
                                                                int64_t K, int8_t* __restrict__ q,
                                                                float* __restrict__ s_out) {
   __shared__ float red[kAqThreads / 32];
+  // Launched with programmatic serialization: wait for the previous kernel
+  // (which may produce x or still read q) before touching memory, then let
+  // the next kernel (a GEMM that streams weights first) start.
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t m = blockIdx.x;
   const int64_t nvec = K / 8;
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
@@ -109,10 +114,8 @@ cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
                              cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(M));
   if (K <= static_cast<int64_t>(kAqThreads) * kAqVecPerThread * 8)
-    act_quant_kernel<true><<<grid, kAqThreads, 0, stream>>>(x, K, q, s);
-  else
-    act_quant_kernel<false><<<grid, kAqThreads, 0, stream>>>(x, K, q, s);
-  return cudaGetLastError();
+    return launch_pdl(act_quant_kernel<true>, grid, dim3(kAqThreads), 0, stream, x, K, q, s);
+  return launch_pdl(act_quant_kernel<false>, grid, dim3(kAqThreads), 0, stream, x, K, q, s);
 }
 
 }  // namespace qlin

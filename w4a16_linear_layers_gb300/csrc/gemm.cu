@@ -13,28 +13,41 @@
 // most 128*127*127 < 2^24, so the fp32 accumulator holds the exact integer
 // group partial.
 //
-// Structure (one persistent block of 512 threads per SM):
+// Structure (one persistent block of 640 threads per SM):
 //   * the output is cut into tiles of 128 features x T tokens; the MMA runs
-//     with the weights as operand A (128 rows = features, held in TMEM) and
-//     the tokens as operand B (T columns, in shared memory), so decode-sized
-//     M only pads T up to a multiple of 16;
+//     with the weights as operand A (128 rows = features, converted by
+//     threads straight into TMEM) and the tokens as operand B (T columns,
+//     16-bit, loaded by TMA with 128-byte swizzle), so decode-sized M only
+//     pads T up to a multiple of 16;
+//   * W8A8 activations are turned from int8 into fp16 once per call by a
+//     small pre-pass kernel (exact), so the GEMM's B operand path is the same
+//     for both formats and no block converts activations;
 //   * the work is the list of (tile, group) steps; block c takes the
 //     contiguous range [c*W/C, (c+1)*W/C) of the W steps (stream-K), so every
 //     SM gets the same amount of weight stream whatever the shape;
 //   * a tile split between blocks is finished by the last block to arrive on
 //     its counter, which sums the per-block fp32 partials in ascending block
 //     order (deterministic, no spin waits);
-//   * warp 0 issues TMA loads into a ring of stages, warp 1 allocates TMEM and
-//     issues the MMAs, the converter warps unpack weights (and, for W8A8, the
-//     int8 activations) into MMA operands, the epilogue warps drain TMEM.
+//   * roles: warp 0 streams weights by TMA, warp 2 streams activations and
+//     group scales, warps 1 and 3 issue the MMAs of alternate steps (one
+//     thread's issue rate is below what the weight stream needs), warps 4-11
+//     convert weights into TMEM, warps 12-19 drain TMEM.
 //
 // W8A8 per group g:  D = A_g * B_g (exact integers), then acc = fma(D, s_w, acc)
 // in the epilogue, ascending g; at the end y = bf16(acc * s_a).
-// W4A16: A = bf16(q * s) per weight; D accumulates over all K in TMEM; y = bf16(D).
+// W4A16: A = bf16(q * s) per weight; D accumulates over all K in TMEM (one
+// accumulator per MMA issuer, summed in the epilogue); y = bf16(D).
 //
 // Every wait is bounded (qlin_device.cuh); a wait that runs out records an
 // error, aborts the block's pipeline and the block still drains its TMA
 // loads and MMAs and frees its TMEM before it exits.
+//
+// Launches use programmatic dependent launch: a kernel lets the next one start
+// early and every kernel waits for its predecessor (griddepcontrol.wait)
+// before it touches anything the predecessor may produce or consume
+// (activations, outputs, workspace).  Weights and scales are read without
+// waiting; the packer, which writes weights, never lets its successor start
+// early.
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
@@ -48,11 +61,14 @@
 namespace qlin {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
 constexpr int kTileF = 128;            // features per tile = MMA M
 constexpr uint32_t kSmemLimit = 232448; // 227 KB opt-in shared memory per block
 constexpr uint32_t kCtrlBytes = 1024;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 10;
+constexpr size_t kCounterBytes = 4096;   // int counters for up to 1024 blocks
+constexpr int64_t kMinSteps = 8;          // minimum (tile, group) steps per block
+constexpr int kScaleChunk = 8;            // groups of scales per TMA load
 
 constexpr int kModeW8A8 = 0;
 constexpr int kModeP = 1;     // W8A8 pipeline, exports the group partials
@@ -61,30 +77,55 @@ constexpr int kModeW4 = 2;
 template <int kMode, int T>
 struct Cfg {
   static constexpr bool kW4 = kMode == kModeW4;
+  // warps 0..3: control (0 weight TMA, 1 TMEM owner + MMA issuer, 2 activation
+  //             and scale TMA, 3 MMA issuer)
+  // warps 4..11: converters, two groups of four (each group converts half of
+  //              every 128-wide K group; warp w serves TMEM lanes 32*(w%4)..)
+  // warps 12..19: epilogue, two groups of four (each drains half of the T
+  //              token columns of the accumulator)
   static constexpr int kConvWarp0 = 4;
-  static constexpr int kConvWarps = kW4 ? 8 : 4;
-  static constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
-  static constexpr int kEpiWarps = 16 - kEpiWarp0;
+  static constexpr int kConvWarps = 8;
+  static constexpr int kEpiWarp0 = 12;
+  static constexpr int kEpiWarps = 8;
   static constexpr int kConvThreads = 32 * kConvWarps;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kWordRows = kW4 ? 16 : 32;           // int32 rows per group
   static constexpr uint32_t kWBytes = kWordRows * kTileF * 4;
-  static constexpr uint32_t kABytes = kW4 ? 2u * T * 128u : T * 128u;
+  static constexpr uint32_t kABytes = 2u * T * 128u;         // two 64-wide 16-bit halves
   static constexpr uint32_t kStageBytes = (kWBytes + kABytes + 1023u) & ~1023u;
-  static constexpr uint32_t kBBytes = kW4 ? 0u : T * 256u;  // converted fp16 B, per buffer
-  static constexpr uint32_t kBTotal = 2u * kBBytes;
-  static constexpr uint32_t kTmemCols = (128 + 2 * T) <= 256 ? 256u : 512u;
-  static constexpr uint32_t kColA = 0;      // two A buffers of 64 columns
-  static constexpr uint32_t kColD = 128;    // two D buffers of T columns
-  static constexpr int kEpiCols = kW4 ? T : T / 2;           // columns per epilogue thread
-  static constexpr uint32_t kEmptyCount = kW4 ? kConvThreads + 1 : kConvThreads;
+  static constexpr int kIssuers = 2;
+  // W4A16 accumulates a whole segment in TMEM: one accumulator per issuer
+  // and segment buffer (two segment buffers while they fit).
+  static constexpr int kSegBufs = kW4 ? (T <= 96 ? 2 : 1) : 0;
+  static constexpr int kW4DCols = kW4 ? kSegBufs * kIssuers * T : 0;
+  // A (64 TMEM columns) and, for W8A8, D (T columns) buffers in flight
+  // between the converters, the MMA issuers and the epilogue.
+  static constexpr int kNumBufRaw = kW4 ? (512 - kW4DCols) / 64 : 512 / (64 + T);
+  static constexpr int kNumBuf = kNumBufRaw < 4 ? kNumBufRaw : 4;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColA = 0;
+  static constexpr uint32_t kColD = 64 * kNumBuf;
+  static constexpr int kEpiCols = T / 2;                     // columns per epilogue thread
+  // a stage is released by the converters (weights) and the MMA (activations)
+  static constexpr uint32_t kEmptyCount = kConvWarps + 1;
+  // Group scales travel by TMA into a ring of their own (kScaleChunk groups x
+  // 128 x 16-bit per slot), read by the epilogue (W8A8) or the converters
+  // (W4A16).
+  static constexpr bool kScales = kMode != kModeP;
+  static constexpr int kScaleSlots = 4;
+  static constexpr uint32_t kScaleSlotBytes = kScaleChunk * 256u;
+  static constexpr uint32_t kScaleBytes = kScales ? kScaleSlots * kScaleSlotBytes : 0u;
   static_assert(T % 16 == 0 && T >= 16 && T <= 128, "token tile");
   static_assert(kEpiCols % 8 == 0, "epilogue columns");
+  static_assert(kNumBuf >= 2, "double buffering at least");
+  static_assert(kColD + (kW4 ? kW4DCols : kNumBuf * T) <= kTmemCols, "TMEM budget");
+  static_assert(kConvThreads == 256 && kEpiThreads == 256, "warp roles");
 };
+
+constexpr int kBufMax = 4;
 
 struct KParams {
   const float* s_a;
-  const uint16_t* scales;
   void* out;
   int64_t M, N, G, F, W;
   float* part;
@@ -94,14 +135,16 @@ struct KParams {
   int stages;
 };
 
-// Shared control block (after the stage ring and the B buffers).
+// Shared control block (after the stage ring and the scale ring).
 struct Ctrl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t a_full[2];
-  uint64_t a_empty[2];
-  uint64_t d_full[2];
-  uint64_t d_empty[2];
+  uint64_t a_full[kBufMax];
+  uint64_t a_empty[kBufMax];
+  uint64_t d_full[kBufMax];
+  uint64_t d_empty[kBufMax];
+  uint64_t s_full[4];
+  uint64_t s_empty[4];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -111,6 +154,59 @@ struct Ctrl {
 __device__ __forceinline__ int64_t cta_of_step(int64_t s, int64_t C, int64_t W) {
   return ((s + 1) * C + W - 1) / W - 1;
 }
+
+// Walks a block's (tile, group) steps without dividing: g is the group, f the
+// feature tile and t the token tile of the current step.
+struct StepIter {
+  int64_t G, F, g, f, t;
+  __device__ __forceinline__ StepIter(int64_t s0, int64_t G_, int64_t F_) : G(G_), F(F_) {
+    const int64_t tile = s0 / G;
+    g = s0 - tile * G;
+    t = tile / F;
+    f = tile - t * F;
+  }
+  __device__ __forceinline__ int64_t tile() const { return t * F + f; }
+  __device__ __forceinline__ void next() {
+    if (++g == G) {
+      g = 0;
+      if (++f == F) {
+        f = 0;
+        ++t;
+      }
+    }
+  }
+};
+
+// Position in a ring of n slots: slot index and the parity of its phase.
+struct Ring {
+  int n, slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ explicit Ring(int n_) : n(n_) {}
+  __device__ __forceinline__ void next() {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Scale chunks: a segment (one block's run of groups of one tile) is cut into
+// chunks of kScaleChunk groups, each brought in by one TMA load.
+struct ChunkIter {
+  int cg = 0;      // group offset inside the current segment
+  int ci = -1;     // chunk counter
+  __device__ __forceinline__ bool begin(bool seg_first) {
+    if (seg_first) cg = 0;
+    const bool starts = (cg % kScaleChunk) == 0;
+    if (starts) ++ci;
+    return starts;
+  }
+  __device__ __forceinline__ int row() const { return cg % kScaleChunk; }
+  __device__ __forceinline__ bool ends(bool seg_last) const {
+    return seg_last || (cg % kScaleChunk) == kScaleChunk - 1;
+  }
+  __device__ __forceinline__ void advance() { ++cg; }
+};
 
 // Four bf16 pairs of one int4 word: nibble i holds q_i + 8 for k = 8kk + i.
 // Output word j holds (k = 2j, 2j+1) as bf16(q * s), rounded once.
@@ -129,18 +225,91 @@ __device__ __forceinline__ void int4x8_to_bf16x8(uint32_t w, uint32_t s2, uint32
   }
 }
 
+// All lanes of the warp agree on a wait's outcome.
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xFFFFFFFFu, ok); }
+
+// Finish a block's segment of a tile whose K was split across blocks: publish
+// this block's fp32 partial, count the arrival on the counter of the tile's
+// first contributing block, and if this block is the last to arrive, sum every
+// contributor's partial in ascending block order into `vals`.  Returns true
+// when `vals` now holds the whole tile's sum (this block writes the output).
+// Ordering: the epilogue threads' partial stores are ordered before thread 0's
+// release by the barrier; the acquire half of the same atomic, followed by
+// the barrier, orders the last block's reads after every contributor's stores.
+template <int kCols>
+__device__ __forceinline__ bool split_tile_fixup(const KParams& p, Ctrl* ctrl, int64_t tile,
+                                                 int64_t cta, int64_t nC, int64_t first_tile,
+                                                 int colbase, int r, int et, int epi_threads,
+                                                 float* vals) {
+  const int64_t G = p.G;
+  const int slot = (tile == first_tile) ? 0 : 1;
+  float* mine = p.part + ((cta * 2 + slot) * (2 * kCols)) * kTileF;
+#pragma unroll
+  for (int c = 0; c < kCols; ++c) mine[(colbase + c) * kTileF + r] = vals[c];
+  named_bar_sync(1, epi_threads);
+  const int64_t c_first = cta_of_step(tile * G, nC, p.W);
+  const int64_t c_last = cta_of_step(tile * G + G - 1, nC, p.W);
+  if (et == 0) {
+    const int old = atomic_add_acq_rel_gpu(&p.counters[c_first], 1);
+    ctrl->last_flag = (old == static_cast<int>(c_last - c_first)) ? 1 : 0;
+  }
+  named_bar_sync(1, epi_threads);
+  if (!ctrl->last_flag) return false;
+  // Sum in ascending contributor order; loads of several contributors are in
+  // flight at once (8 columns at a time) to hide the L2 round trips.
+  auto part_of = [&](int64_t cc) {
+    const int slot2 = ((cc * p.W / nC) / G == tile) ? 0 : 1;
+    return p.part + ((cc * 2 + slot2) * (2 * kCols)) * kTileF + static_cast<int64_t>(colbase) * kTileF + r;
+  };
+  constexpr int kC8 = kCols < 8 ? kCols : 8;
+  constexpr int kU = kCols <= 16 ? 4 : 2;     // contributors in flight
+#pragma unroll
+  for (int c0 = 0; c0 < kCols; c0 += kC8) {
+    float sum[kC8];
+#pragma unroll
+    for (int c = 0; c < kC8; ++c) sum[c] = 0.0f;
+    int64_t cc = c_first;
+    for (; cc + kU - 1 <= c_last; cc += kU) {
+      float v[kU][kC8];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const float* pp = part_of(cc + u);
+#pragma unroll
+        for (int c = 0; c < kC8; ++c) v[u][c] = __ldcg(pp + (c0 + c) * kTileF);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int c = 0; c < kC8; ++c) sum[c] += v[u][c];
+    }
+    for (; cc <= c_last; ++cc) {
+      const float* pp = part_of(cc);
+#pragma unroll
+      for (int c = 0; c < kC8; ++c) sum[c] += __ldcg(pp + (c0 + c) * kTileF);
+    }
+#pragma unroll
+    for (int c = 0; c < kC8; ++c) vals[c0 + c] = sum[c];
+  }
+  if (et == 0) p.counters[c_first] = 0;
+  return true;
+}
+
 template <int kMode, int T>
 __global__ void __launch_bounds__(kThreads, 1)
     qlin_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
-                     const __grid_constant__ CUtensorMap tm_a, const KParams p) {
+                     const __grid_constant__ CUtensorMap tm_a,
+                     const __grid_constant__ CUtensorMap tm_s, const KParams p) {
   using C = Cfg<kMode, T>;
+  constexpr int NB = C::kNumBuf;
+  constexpr int SR = C::kScaleSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const int stages = p.stages;
-  const uint32_t b_off = static_cast<uint32_t>(stages) * C::kStageBytes;
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + b_off + C::kBTotal);
+  const uint32_t sc_off = static_cast<uint32_t>(stages) * C::kStageBytes;
+  const uint16_t* scale_ring = reinterpret_cast<const uint16_t*>(smem + sc_off);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + sc_off + C::kScaleBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -151,23 +320,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_steps = static_cast<int>(s1 - s0);
   const int64_t G = p.G;
   const int64_t F = p.F;
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_a = policy_evict_last();
+  int w_issued = 0;   // weight loads issued by the weight producer (warp 0, lane 0)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
-      mbar_init(smem_u32(&ctrl->full[i]), 1);
+      mbar_init(smem_u32(&ctrl->full[i]), 2);      // weight producer + activation producer
       mbar_init(smem_u32(&ctrl->empty[i]), C::kEmptyCount);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&ctrl->a_full[i]), C::kConvThreads);
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(smem_u32(&ctrl->a_full[i]), C::kConvWarps);
       mbar_init(smem_u32(&ctrl->a_empty[i]), 1);
-      mbar_init(smem_u32(&ctrl->d_full[i]), 1);
-      mbar_init(smem_u32(&ctrl->d_empty[i]), C::kEpiThreads);
+      mbar_init(smem_u32(&ctrl->d_full[i]), C::kW4 ? C::kIssuers : 1);
+      mbar_init(smem_u32(&ctrl->d_empty[i]), C::kEpiWarps);
     }
-    mbar_init(smem_u32(&ctrl->mma_done), 1);
+    for (int i = 0; i < SR; ++i) {
+      mbar_init(smem_u32(&ctrl->s_full[i]), 1);
+      mbar_init(smem_u32(&ctrl->s_empty[i]), 8);
+    }
+    mbar_init(smem_u32(&ctrl->mma_done), C::kIssuers);
     ctrl->abort_flag = 0;
     ctrl->last_flag = 0;
     fence_barrier_init();
+    // The weights depend on nothing: start streaming them before the block's
+    // set-up barrier (every stage is free, so no wait is needed).
+    prefetch_tmap(&tm_w);
+    StepIter it(s0, G, F);
+    const int first = n_steps < stages ? n_steps : stages;
+    for (int j = 0; j < first; ++j, it.next()) {
+      const uint32_t full = smem_u32(&ctrl->full[j]);
+      mbar_arrive_expect_tx(full, C::kWBytes);
+      tma_load_2d(sbase + static_cast<uint32_t>(j) * C::kStageBytes, &tm_w, full,
+                  static_cast<int32_t>(it.f * kTileF), static_cast<int32_t>(it.g * C::kWordRows),
+                  pol_w);
+    }
+    w_issued = first;
   }
+  __syncwarp();
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctrl->tmem_base), C::kTmemCols);
     tmem_relinquish();
@@ -175,366 +365,334 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_launch();
   const uint32_t tmem = ctrl->tmem_base;
   const WaitCtx ctx{p.err, &ctrl->abort_flag, p.limit_ns};
   int never_abort = 0;
   const WaitCtx drain_ctx{p.err, &never_abort, p.limit_ns};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------ weight producer
     if (lane == 0) {
-      prefetch_tmap(&tm_w);
-      prefetch_tmap(&tm_a);
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_a = policy_evict_last();
-      int issued = 0;
-      for (int j = 0; j < n_steps; ++j) {
-        const int st = j % stages;
-        const uint32_t ph = static_cast<uint32_t>(j / stages) & 1u;
-        if (!mbar_wait(smem_u32(&ctrl->empty[st]), ph ^ 1u, ctx, 1)) break;
-        const int64_t s = s0 + j;
-        const int64_t tile = s / G;
-        const int64_t g = s - tile * G;
-        const int64_t t = tile / F;
-        const int64_t f = tile - t * F;
-        const uint32_t full = smem_u32(&ctrl->full[st]);
-        const uint32_t dst = sbase + static_cast<uint32_t>(st) * C::kStageBytes;
-        mbar_arrive_expect_tx(full, C::kWBytes + C::kABytes);
-        tma_load_2d(dst, &tm_w, full, static_cast<int32_t>(f * kTileF),
-                    static_cast<int32_t>(g * C::kWordRows), pol_w);
-        if constexpr (C::kW4) {
-          tma_load_2d(dst + C::kWBytes, &tm_a, full, static_cast<int32_t>(g * kGroup),
-                      static_cast<int32_t>(t * T), pol_a);
-          tma_load_2d(dst + C::kWBytes + T * 128u, &tm_a, full,
-                      static_cast<int32_t>(g * kGroup + 64), static_cast<int32_t>(t * T), pol_a);
-        } else {
-          tma_load_2d(dst + C::kWBytes, &tm_a, full, static_cast<int32_t>(g * kGroup),
-                      static_cast<int32_t>(t * T), pol_a);
-        }
-        ++issued;
+      StepIter it(s0, G, F);
+      Ring rg(stages);
+      for (int j = 0; j < w_issued; ++j) {
+        it.next();
+        rg.next();
+      }
+      for (int j = w_issued; j < n_steps; ++j, it.next(), rg.next()) {
+        if (!mbar_wait(smem_u32(&ctrl->empty[rg.slot]), rg.phase ^ 1u, ctx, 1)) break;
+        const uint32_t full = smem_u32(&ctrl->full[rg.slot]);
+        mbar_arrive_expect_tx(full, C::kWBytes);
+        tma_load_2d(sbase + static_cast<uint32_t>(rg.slot) * C::kStageBytes, &tm_w, full,
+                    static_cast<int32_t>(it.f * kTileF), static_cast<int32_t>(it.g * C::kWordRows),
+                    pol_w);
+        ++w_issued;
       }
       // Every load issued must land before the block exits.
-      for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
+      for (int j = w_issued > stages ? w_issued - stages : 0; j < w_issued; ++j)
         (void)mbar_wait(smem_u32(&ctrl->full[j % stages]),
                         static_cast<uint32_t>(j / stages) & 1u, drain_ctx, 2);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------ activation and scale producer
     if (lane == 0) {
+      prefetch_tmap(&tm_a);
+      if constexpr (C::kScales) prefetch_tmap(&tm_s);
+      StepIter it(s0, G, F);
+      Ring rg(stages);
+      ChunkIter ch;
+      int issued = 0, s_issued = 0;
+      bool waited = false;
+      for (int j = 0; j < n_steps; ++j, it.next(), rg.next(), ch.advance()) {
+        if constexpr (C::kScales) {
+          if (ch.begin(j == 0 || it.g == 0)) {
+            const int slot = ch.ci % SR;
+            const uint32_t sph = static_cast<uint32_t>(ch.ci / SR) & 1u;
+            if (!mbar_wait(smem_u32(&ctrl->s_empty[slot]), sph ^ 1u, ctx, 11)) break;
+            const uint32_t sfull = smem_u32(&ctrl->s_full[slot]);
+            mbar_arrive_expect_tx(sfull, C::kScaleSlotBytes);
+            tma_load_2d(sbase + sc_off + static_cast<uint32_t>(slot) * C::kScaleSlotBytes, &tm_s,
+                        sfull, static_cast<int32_t>(it.f * kTileF), static_cast<int32_t>(it.g),
+                        pol_w);
+            ++s_issued;
+          }
+        }
+        if (!mbar_wait(smem_u32(&ctrl->empty[rg.slot]), rg.phase ^ 1u, ctx, 15)) break;
+        if (!waited) {
+          grid_dep_wait();   // the activations come from the previous kernel
+          waited = true;
+        }
+        const uint32_t full = smem_u32(&ctrl->full[rg.slot]);
+        const uint32_t dst = sbase + static_cast<uint32_t>(rg.slot) * C::kStageBytes + C::kWBytes;
+        mbar_arrive_expect_tx(full, C::kABytes);
+        tma_load_2d(dst, &tm_a, full, static_cast<int32_t>(it.g * kGroup),
+                    static_cast<int32_t>(it.t * T), pol_a);
+        tma_load_2d(dst + T * 128u, &tm_a, full, static_cast<int32_t>(it.g * kGroup + 64),
+                    static_cast<int32_t>(it.t * T), pol_a);
+        ++issued;
+      }
+      for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
+        (void)mbar_wait(smem_u32(&ctrl->full[j % stages]),
+                        static_cast<uint32_t>(j / stages) & 1u, drain_ctx, 16);
+      for (int c = s_issued > SR ? s_issued - SR : 0; c < s_issued; ++c)
+        (void)mbar_wait(smem_u32(&ctrl->s_full[c % SR]), static_cast<uint32_t>(c / SR) & 1u,
+                        drain_ctx, 12);
+    }
+    __syncwarp();
+  } else if (warp == 1 || warp == 3) {
+    // ----------------------------------------------------------- MMA issuers
+    // warp 1 takes the even steps, warp 3 the odd ones
+    if (lane == 0) {
+      const int me = warp == 1 ? 0 : 1;
       constexpr uint32_t idesc = idesc_f16(kTileF, T, C::kW4);
+      StepIter it(s0, G, F);
+      Ring rg(stages);
       int seg = 0;
-      for (int j = 0; j < n_steps; ++j) {
-        const int ab = j & 1;
-        const uint32_t abph = static_cast<uint32_t>(j >> 1) & 1u;
-        if constexpr (C::kW4) {
-          const int64_t s = s0 + j;
-          const int64_t g = s % G;
-          const bool first = (j == 0) || (g == 0);
-          const bool last = (s == s1 - 1) || (g == G - 1);
-          const int st = j % stages;
-          const uint32_t ph = static_cast<uint32_t>(j / stages) & 1u;
-          const int db = seg & 1;
-          const uint32_t dbph = static_cast<uint32_t>(seg >> 1) & 1u;
-          if (!mbar_wait(smem_u32(&ctrl->full[st]), ph, ctx, 3)) break;
+      bool started = false;   // W4A16: this issuer has accumulated into the segment
+      for (int j = 0; j < n_steps; ++j, it.next(), rg.next()) {
+        const bool seg_first = (j == 0) || (it.g == 0);
+        const bool seg_last = (j == n_steps - 1) || (it.g == G - 1);
+        const int ab = j % NB;
+        const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
+        if (seg_first) started = false;
+        const int db = C::kW4 ? seg % C::kSegBufs : ab;
+        const uint32_t dbph = C::kW4 ? (static_cast<uint32_t>(seg / C::kSegBufs) & 1u) : abph;
+        const uint32_t dcol = C::kW4 ? tmem + C::kColD + (db * C::kIssuers + me) * T
+                                     : tmem + C::kColD + ab * T;
+        if ((j & 1) == me) {
+          const bool need_d = C::kW4 ? !started : true;
+          if (!mbar_wait(smem_u32(&ctrl->full[rg.slot]), rg.phase, ctx, 3)) break;
           if (!mbar_wait(smem_u32(&ctrl->a_full[ab]), abph, ctx, 4)) break;
-          if (first && !mbar_wait(smem_u32(&ctrl->d_empty[db]), dbph ^ 1u, ctx, 5)) break;
+          if (need_d && !mbar_wait(smem_u32(&ctrl->d_empty[db]), dbph ^ 1u, ctx, 5)) break;
           tc_fence_after();
-          const uint32_t xb = sbase + static_cast<uint32_t>(st) * C::kStageBytes + C::kWBytes;
+          const uint32_t xb =
+              sbase + static_cast<uint32_t>(rg.slot) * C::kStageBytes + C::kWBytes;
+          const uint64_t d0 = smem_desc(xb, 16u, 1024u, 2u);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t bdesc =
-                smem_desc(xb + static_cast<uint32_t>(ks >> 2) * (T * 128u) +
-                              static_cast<uint32_t>(ks & 3) * 32u,
-                          16u, 1024u, 2u);
-            mma_ts(tmem + C::kColD + db * T, tmem + C::kColA + ab * 64 + ks * 8, bdesc, idesc,
-                   (first && ks == 0) ? 0u : 1u);
+            // 128-byte swizzled K-major 16-bit tile: 8-row groups 1024 B
+            // apart, K advanced by 32 B (16 elements) inside the 128-byte row;
+            // the second 64-wide half of the group starts T*128 B further.
+            const uint32_t off = static_cast<uint32_t>(ks >> 2) * (T * 128u) +
+                                 static_cast<uint32_t>(ks & 3) * 32u;
+            const bool acc = C::kW4 ? (started || ks > 0) : ks > 0;
+            mma_ts(dcol, tmem + C::kColA + ab * 64 + ks * 8, d0 + (off >> 4), idesc,
+                   acc ? 1u : 0u);
           }
           tc_commit(smem_u32(&ctrl->a_empty[ab]));
-          tc_commit(smem_u32(&ctrl->empty[st]));
-          if (last) {
-            tc_commit(smem_u32(&ctrl->d_full[db]));
+          tc_commit(smem_u32(&ctrl->empty[rg.slot]));
+          if constexpr (!C::kW4) tc_commit(smem_u32(&ctrl->d_full[ab]));
+          started = true;
+        }
+        if constexpr (C::kW4) {
+          if (seg_last) {
+            // Every issuer reports on every segment.  One that accumulated
+            // nothing into it arrives directly, but only once the epilogue has
+            // released this buffer's previous segment, so that its arrival
+            // cannot complete that earlier phase in the other issuer's place.
+            if (started) {
+              tc_commit(smem_u32(&ctrl->d_full[db]));
+            } else {
+              if (!mbar_wait(smem_u32(&ctrl->d_empty[db]), dbph ^ 1u, ctx, 17)) break;
+              mbar_arrive(smem_u32(&ctrl->d_full[db]));
+            }
             ++seg;
           }
-        } else {
-          if (!mbar_wait(smem_u32(&ctrl->a_full[ab]), abph, ctx, 3)) break;
-          if (!mbar_wait(smem_u32(&ctrl->d_empty[ab]), abph ^ 1u, ctx, 4)) break;
-          tc_fence_after();
-          const uint32_t bb = sbase + b_off + static_cast<uint32_t>(ab) * C::kBBytes;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            // canonical K-major, no swizzle: core matrices of 8 rows x 16 B;
-            // LBO = 128 B between K-adjacent core matrices, SBO = 2048 B
-            // between 8-row groups.
-            const uint64_t bdesc = smem_desc(bb + static_cast<uint32_t>(ks) * 256u, 128u, 2048u, 0u);
-            mma_ts(tmem + C::kColD + ab * T, tmem + C::kColA + ab * 64 + ks * 8, bdesc, idesc,
-                   ks > 0 ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&ctrl->a_empty[ab]));
-          tc_commit(smem_u32(&ctrl->d_full[ab]));
         }
       }
       tc_commit(smem_u32(&ctrl->mma_done));
       (void)mbar_wait(smem_u32(&ctrl->mma_done), 0u, drain_ctx, 6);
     }
+    __syncwarp();
   } else if (warp >= C::kConvWarp0 && warp < C::kEpiWarp0) {
     // ------------------------------------------------------------ converters
-    const int ct = threadIdx.x - 32 * C::kConvWarp0;
-    const int r = ct & 127;                      // row of A = TMEM lane
+    const int ct = threadIdx.x - 32 * C::kConvWarp0;      // 0..255
+    const int kh = ct >> 7;                                // half of the group's K
+    const int r = ct & 127;                                // row of A = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    for (int j = 0; j < n_steps; ++j) {
-      const int st = j % stages;
-      const uint32_t ph = static_cast<uint32_t>(j / stages) & 1u;
-      const int ab = j & 1;
-      const uint32_t abph = static_cast<uint32_t>(j >> 1) & 1u;
-      bool ok = mbar_wait(smem_u32(&ctrl->full[st]), ph, ctx, 7);
+    StepIter it(s0, G, F);
+    Ring rg(stages);
+    ChunkIter ch;
+    for (int j = 0; j < n_steps; ++j, it.next(), rg.next(), ch.advance()) {
+      const int ab = j % NB;
+      const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
+      bool ok = mbar_wait(smem_u32(&ctrl->full[rg.slot]), rg.phase, ctx, 7);
       if (ok) ok = mbar_wait(smem_u32(&ctrl->a_empty[ab]), abph ^ 1u, ctx, 8);
-      if (!named_bar_and(3, C::kConvThreads, ok)) break;
-      tc_fence_after();
-      const uint8_t* stage = smem + static_cast<uint32_t>(st) * C::kStageBytes;
-      const uint32_t* wsm = reinterpret_cast<const uint32_t*>(stage);
-      const uint32_t acol = tmem + lane_off + C::kColA + ab * 64;
+      uint32_t s2 = 0;
       if constexpr (C::kW4) {
-        const int kh = ct >> 7;                  // which half of the group's K
-        const int64_t s = s0 + j;
-        const int64_t tile = s / G;
-        const int64_t g = s - tile * G;
-        const int64_t n = (tile % F) * kTileF + r;
-        uint32_t s2 = 0;
-        if (n < p.N) {
-          const uint32_t sb = p.scales[g * p.N + n];
-          s2 = sb | (sb << 16);
+        const bool seg_last = (j == n_steps - 1) || (it.g == G - 1);
+        ch.begin(j == 0 || it.g == 0);
+        const int slot = ch.ci % SR;
+        if (ok && ch.row() == 0)
+          ok = mbar_wait(smem_u32(&ctrl->s_full[slot]), static_cast<uint32_t>(ch.ci / SR) & 1u,
+                         ctx, 13);
+        if (!warp_all(ok)) break;
+        const uint32_t sb = scale_ring[(slot * kScaleChunk + ch.row()) * 128 + r];
+        s2 = sb | (sb << 16);
+        if (ch.ends(seg_last)) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->s_empty[slot]));
         }
+      } else {
+        if (!warp_all(ok)) break;
+      }
+      tc_fence_after();
+      const uint32_t* wsm =
+          reinterpret_cast<const uint32_t*>(smem + static_cast<uint32_t>(rg.slot) * C::kStageBytes);
+      const uint32_t acol = tmem + lane_off + C::kColA + ab * 64 + kh * 32;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t v[16];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[16];
+        if constexpr (C::kW4) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             int4x8_to_bf16x8(wsm[(kh * 8 + h * 4 + i) * kTileF + r], s2, v + 4 * i);
-          tmem_st16(acol + kh * 32 + h * 16, v);
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t v[16];
+        } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            biased_u8x4_to_f16x4(wsm[(h * 8 + i) * kTileF + r], v[2 * i], v[2 * i + 1]);
-          tmem_st16(acol + h * 16, v);
+            biased_u8x4_to_f16x4(wsm[(kh * 16 + h * 8 + i) * kTileF + r], v[2 * i], v[2 * i + 1]);
         }
-        // int8 activations (128-byte swizzled TMA tile, T rows x 128 B) ->
-        // fp16 canonical layout in B buffer ab.
-        const uint8_t* araw = stage + C::kWBytes;
-        uint8_t* bbuf = smem + b_off + static_cast<uint32_t>(ab) * C::kBBytes;
-#pragma unroll
-        for (int i = 0; i < T / 16; ++i) {
-          const int x = ct + 128 * i;
-          const int cc = x / T;
-          const int rr = x - cc * T;
-          const uint4 raw =
-              *reinterpret_cast<const uint4*>(araw + rr * 128 + ((cc ^ (rr & 7)) << 4));
-          uint4 o0, o1;
-          biased_u8x4_to_f16x4(raw.x ^ 0x80808080u, o0.x, o0.y);
-          biased_u8x4_to_f16x4(raw.y ^ 0x80808080u, o0.z, o0.w);
-          biased_u8x4_to_f16x4(raw.z ^ 0x80808080u, o1.x, o1.y);
-          biased_u8x4_to_f16x4(raw.w ^ 0x80808080u, o1.z, o1.w);
-          uint8_t* dst = bbuf + (rr >> 3) * 2048 + (rr & 7) * 16 + cc * 256;
-          *reinterpret_cast<uint4*>(dst) = o0;
-          *reinterpret_cast<uint4*>(dst + 128) = o1;
-        }
-        fence_proxy_async_smem();
+        tmem_st16(acol + h * 16, v);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&ctrl->empty[st]));
-      mbar_arrive(smem_u32(&ctrl->a_full[ab]));
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&ctrl->empty[rg.slot]));
+        mbar_arrive(smem_u32(&ctrl->a_full[ab]));
+      }
     }
+    __syncwarp();
   } else if (warp >= C::kEpiWarp0) {
     // ------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 32 * C::kEpiWarp0;
-    const int r = (warp & 3) * 32 + lane;        // TMEM lane = feature in tile
+    const int et = threadIdx.x - 32 * C::kEpiWarp0;        // 0..255
+    const int r = (warp & 3) * 32 + lane;                  // TMEM lane = feature in tile
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int colbase = C::kW4 ? 0 : ((warp - C::kEpiWarp0) >> 2) * (T / 2);
+    const int colbase = ((warp - C::kEpiWarp0) >> 2) * C::kEpiCols;
+    constexpr int kCh = C::kEpiCols < 16 ? C::kEpiCols : 16;
     const int64_t M = p.M, N = p.N;
     const int64_t first_tile = s0 / G;
     uint16_t* y = static_cast<uint16_t*>(p.out);
-
-    if constexpr (!C::kW4) {
-      float acc[C::kEpiCols];
-      int64_t seg_g0 = 0;
-      for (int j = 0; j < n_steps; ++j) {
-        const int64_t s = s0 + j;
-        const int64_t tile = s / G;
-        const int64_t g = s - tile * G;
-        const int64_t t = tile / F;
-        const int64_t f = tile - t * F;
-        const int64_t n = f * kTileF + r;
-        if (j == 0 || g == 0) {
-          seg_g0 = g;
+    float acc[C::kEpiCols];
+    bool alive = true;          // false once this warp's waits gave up
+    int64_t seg_g0 = 0;
+    int seg = 0;
+    int seg_j0 = 0;             // first step of the current segment
+    bool waited = false;
+    StepIter it(s0, G, F);
+    ChunkIter ch;
+    for (int j = 0; j < n_steps; ++j, it.next(), ch.advance()) {
+      const int64_t g = it.g, t = it.t;
+      const int64_t n = it.f * kTileF + r;
+      const bool seg_first = (j == 0) || (g == 0);
+      const bool seg_last = (j == n_steps - 1) || (g == G - 1);
+      if (seg_first) {
+        seg_g0 = g;
+        seg_j0 = j;
 #pragma unroll
-          for (int c = 0; c < C::kEpiCols; ++c) acc[c] = 0.0f;
-        }
-        const int b = j & 1;
-        const uint32_t bph = static_cast<uint32_t>(j >> 1) & 1u;
+        for (int c = 0; c < C::kEpiCols; ++c) acc[c] = 0.0f;
+      }
+      if (!C::kW4 || seg_last) {
+        // drain one accumulator buffer: per group (W8A8) or per segment (W4A16)
+        const int nbuf = C::kW4 ? C::kSegBufs : NB;
+        const int idx = C::kW4 ? seg : j;
+        const int b = idx % nbuf;
+        const uint32_t bph = static_cast<uint32_t>(idx / nbuf) & 1u;
         float sw = 0.0f;
-        if (kMode == kModeW8A8 && n < N)
-          sw = __half2float(__ushort_as_half(p.scales[g * N + n]));
-        const bool ok = mbar_wait(smem_u32(&ctrl->d_full[b]), bph, ctx, 9);
-        if (!named_bar_and(2, C::kEpiThreads, ok)) break;
-        tc_fence_after();
-        const uint32_t dcol = tmem + lane_off + C::kColD + b * T + colbase;
-        constexpr int kCh = C::kEpiCols < 16 ? C::kEpiCols : 16;
-#pragma unroll
-        for (int c0 = 0; c0 < C::kEpiCols; c0 += kCh) {
-          uint32_t v[kCh];
-          if constexpr (kCh == 16) tmem_ld16(dcol + c0, v);
-          else tmem_ld8(dcol + c0, v);
-          tmem_wait_ld();
-          if constexpr (kMode == kModeP) {
-            int32_t* P = static_cast<int32_t*>(p.out);
-#pragma unroll
-            for (int c = 0; c < kCh; ++c) {
-              const int64_t m = t * T + colbase + c0 + c;
-              if (m < M && n < N)
-                P[(g * M + m) * N + n] = static_cast<int32_t>(__uint_as_float(v[c]));
+        if constexpr (kMode == kModeW8A8) {
+          ch.begin(seg_first);
+          const int slot = ch.ci % SR;
+          if (alive && ch.row() == 0)
+            alive = warp_all(mbar_wait(smem_u32(&ctrl->s_full[slot]),
+                                       static_cast<uint32_t>(ch.ci / SR) & 1u, ctx, 14));
+          if (alive) {
+            sw = __half2float(__ushort_as_half(scale_ring[(slot * kScaleChunk + ch.row()) * 128 + r]));
+            if (ch.ends(seg_last)) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&ctrl->s_empty[slot]));
             }
-          } else {
-#pragma unroll
-            for (int c = 0; c < kCh; ++c) acc[c0 + c] = fmaf(__uint_as_float(v[c]), sw, acc[c0 + c]);
           }
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&ctrl->d_empty[b]));
-
-        if constexpr (kMode == kModeP) {
-          continue;
-        } else {
-          if (!(s == s1 - 1 || g == G - 1)) continue;
-
-          // ---- end of this block's segment of the tile
-          const bool full_tile = (seg_g0 == 0) && (g == G - 1);
-          bool write = full_tile;
-          if (!full_tile) {
-            const int slot = (tile == first_tile) ? 0 : 1;
-            float* mine = p.part + ((cta * 2 + slot) * T) * kTileF;
+        if (alive) alive = warp_all(mbar_wait(smem_u32(&ctrl->d_full[b]), bph, ctx, 9));
+        if (alive) {
+          tc_fence_after();
+          const uint32_t dcol = tmem + lane_off + C::kColD + colbase +
+                                (C::kW4 ? b * C::kIssuers * T : b * T);
 #pragma unroll
-            for (int c = 0; c < C::kEpiCols; ++c) mine[(colbase + c) * kTileF + r] = acc[c];
-            __threadfence();
-            named_bar_sync(1, C::kEpiThreads);
-            const int64_t c_first = cta_of_step(tile * G, nC, p.W);
-            const int64_t c_last = cta_of_step(tile * G + G - 1, nC, p.W);
-            if (et == 0) {
-              const int old = atomicAdd(&p.counters[tile], 1);
-              ctrl->last_flag = (old == static_cast<int>(c_last - c_first)) ? 1 : 0;
-            }
-            named_bar_sync(1, C::kEpiThreads);
-            write = ctrl->last_flag != 0;
-            if (write) {
-              __threadfence();
+          for (int c0 = 0; c0 < C::kEpiCols; c0 += kCh) {
+            uint32_t v[kCh];
+            if constexpr (kCh == 16) tmem_ld16(dcol + c0, v);
+            else tmem_ld8(dcol + c0, v);
+            tmem_wait_ld();
+            if constexpr (C::kW4) {
+              // the issuers' accumulators, summed in issuer order; an issuer
+              // that took no step of this segment left its accumulator unused
+              const bool both = j > seg_j0;
+              const int only = seg_j0 & 1;
+              if (both || only == 0) {
 #pragma unroll
-              for (int c = 0; c < C::kEpiCols; ++c) acc[c] = 0.0f;
-              for (int64_t cc = c_first; cc <= c_last; ++cc) {
-                const int slot2 = ((cc * p.W / nC) / G == tile) ? 0 : 1;
-                const float* pp = p.part + ((cc * 2 + slot2) * T) * kTileF;
-#pragma unroll
-                for (int c = 0; c < C::kEpiCols; ++c) acc[c] += __ldcg(pp + (colbase + c) * kTileF + r);
+                for (int c = 0; c < kCh; ++c) acc[c0 + c] = __uint_as_float(v[c]);
               }
-              if (et == 0) p.counters[tile] = 0;
-            }
-          }
-          if (write && n < N) {
+              if (both || only == 1) {
+                uint32_t v1[kCh];
+                if constexpr (kCh == 16) tmem_ld16(dcol + T + c0, v1);
+                else tmem_ld8(dcol + T + c0, v1);
+                tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < C::kEpiCols; ++c) {
-              const int64_t m = t * T + colbase + c;
-              if (m < M)
-                y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c] * __ldg(p.s_a + m)));
+                for (int c = 0; c < kCh; ++c)
+                  acc[c0 + c] = both ? acc[c0 + c] + __uint_as_float(v1[c]) : __uint_as_float(v1[c]);
+              }
+            } else if constexpr (kMode == kModeP) {
+              if (!waited) {
+                grid_dep_wait();
+                waited = true;
+              }
+              int32_t* P = static_cast<int32_t*>(p.out);
+#pragma unroll
+              for (int c = 0; c < kCh; ++c) {
+                const int64_t m = t * T + colbase + c0 + c;
+                if (m < M && n < N)
+                  P[(g * M + m) * N + n] = static_cast<int32_t>(__uint_as_float(v[c]));
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < kCh; ++c) acc[c0 + c] = fmaf(__uint_as_float(v[c]), sw, acc[c0 + c]);
             }
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->d_empty[b]));
         }
       }
-    } else {
-      int seg = 0;
-      int64_t seg_g0 = 0;
-      for (int j = 0; j < n_steps; ++j) {
-        const int64_t s = s0 + j;
-        const int64_t tile = s / G;
-        const int64_t g = s - tile * G;
-        if (j == 0 || g == 0) seg_g0 = g;
-        if (!(s == s1 - 1 || g == G - 1)) continue;
-        const int64_t t = tile / F;
-        const int64_t f = tile - t * F;
-        const int64_t n = f * kTileF + r;
-        const int db = seg & 1;
-        const uint32_t dbph = static_cast<uint32_t>(seg >> 1) & 1u;
-        ++seg;
-        const bool ok = mbar_wait(smem_u32(&ctrl->d_full[db]), dbph, ctx, 10);
-        if (!named_bar_and(2, C::kEpiThreads, ok)) break;
-        tc_fence_after();
-        const uint32_t dcol = tmem + lane_off + C::kColD + db * T;
-        const bool full_tile = (seg_g0 == 0) && (g == G - 1);
-        if (full_tile) {
+      if (C::kW4 && seg_last) ++seg;
+      if (kMode == kModeP || !seg_last) continue;
+
+      // ---- end of this block's segment of the tile (all epilogue warps agree)
+      if (!named_bar_and(2, C::kEpiThreads, alive)) break;
+      if (!waited) {
+        grid_dep_wait();   // outputs and workspace may still be in use upstream
+        waited = true;
+      }
+      const int64_t tile = it.tile();
+      const bool full_tile = (seg_g0 == 0) && (g == G - 1);
+      bool write = full_tile;
+      if (!full_tile)
+        write = split_tile_fixup<C::kEpiCols>(p, ctrl, tile, cta, nC, first_tile, colbase, r, et,
+                                              C::kEpiThreads, acc);
+      if (write && n < N) {
 #pragma unroll
-          for (int ch = 0; ch < T / 16; ++ch) {
-            uint32_t v[16];
-            tmem_ld16(dcol + ch * 16, v);
-            tmem_wait_ld();
-            if (n < N) {
-#pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const int64_t m = t * T + ch * 16 + c;
-                if (m < M) y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[c])));
-              }
-            }
-          }
-          tc_fence_before();
-          mbar_arrive(smem_u32(&ctrl->d_empty[db]));
-        } else {
-          const int slot = (tile == first_tile) ? 0 : 1;
-          float* mine = p.part + ((cta * 2 + slot) * T) * kTileF;
-#pragma unroll
-          for (int ch = 0; ch < T / 16; ++ch) {
-            uint32_t v[16];
-            tmem_ld16(dcol + ch * 16, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 16; ++c) mine[(ch * 16 + c) * kTileF + r] = __uint_as_float(v[c]);
-          }
-          tc_fence_before();
-          mbar_arrive(smem_u32(&ctrl->d_empty[db]));
-          __threadfence();
-          named_bar_sync(1, C::kEpiThreads);
-          const int64_t c_first = cta_of_step(tile * G, nC, p.W);
-          const int64_t c_last = cta_of_step(tile * G + G - 1, nC, p.W);
-          if (et == 0) {
-            const int old = atomicAdd(&p.counters[tile], 1);
-            ctrl->last_flag = (old == static_cast<int>(c_last - c_first)) ? 1 : 0;
-          }
-          named_bar_sync(1, C::kEpiThreads);
-          if (ctrl->last_flag) {
-            __threadfence();
-#pragma unroll
-            for (int ch = 0; ch < T / 16; ++ch) {
-              float sum[16];
-#pragma unroll
-              for (int c = 0; c < 16; ++c) sum[c] = 0.0f;
-              for (int64_t cc = c_first; cc <= c_last; ++cc) {
-                const int slot2 = ((cc * p.W / nC) / G == tile) ? 0 : 1;
-                const float* pp = p.part + ((cc * 2 + slot2) * T) * kTileF;
-#pragma unroll
-                for (int c = 0; c < 16; ++c) sum[c] += __ldcg(pp + (ch * 16 + c) * kTileF + r);
-              }
-              if (n < N) {
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                  const int64_t m = t * T + ch * 16 + c;
-                  if (m < M) y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum[c]));
-                }
-              }
-            }
-            if (et == 0) p.counters[tile] = 0;
+        for (int c = 0; c < C::kEpiCols; ++c) {
+          const int64_t m = t * T + colbase + c;
+          if (m < M) {
+            const float v = C::kW4 ? acc[c] : acc[c] * __ldg(p.s_a + m);
+            y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
           }
         }
       }
     }
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -543,6 +701,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// int8 activations -> fp16 (exact), 16 values per thread; the W8A8 GEMM's B
+// operand.  Waits for its predecessor before touching memory (the previous
+// GEMM may still read this buffer), then lets the GEMM start.
+__global__ void __launch_bounds__(256) act_i8_to_f16_kernel(const int8_t* __restrict__ q,
+                                                            uint16_t* __restrict__ out,
+                                                            int64_t n16) {
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(q) + i);
+    uint4 o0, o1;
+    biased_u8x4_to_f16x4(raw.x ^ 0x80808080u, o0.x, o0.y);
+    biased_u8x4_to_f16x4(raw.y ^ 0x80808080u, o0.z, o0.w);
+    biased_u8x4_to_f16x4(raw.z ^ 0x80808080u, o1.x, o1.y);
+    biased_u8x4_to_f16x4(raw.w ^ 0x80808080u, o1.z, o1.w);
+    reinterpret_cast<uint4*>(out)[2 * i] = o0;
+    reinterpret_cast<uint4*>(out)[2 * i + 1] = o1;
   }
 }
 
@@ -578,25 +757,46 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+namespace {
+
 template <int kMode, int T>
 cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream_t stream) {
   using C = Cfg<kMode, T>;
+  const void* act16 = a.act;
+  if constexpr (!C::kW4) {
+    // int8 activations -> fp16 image in the workspace
+    uint16_t* dst = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.workspace) + pl.act_offset);
+    const int64_t n16 = a.M * a.K / 16;
+    int64_t blocks = (n16 + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    cudaError_t e = launch_pdl(act_i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256),
+                               0, stream, static_cast<const int8_t*>(a.act), dst, n16);
+    if (e != cudaSuccess) return e;
+    act16 = dst;
+  }
   CUtensorMap tw, ta;
   const uint64_t words_rows = static_cast<uint64_t>(a.K) / (C::kW4 ? 8 : 4);
   if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, a.qweight, a.N, words_rows,
                    static_cast<uint64_t>(a.N) * 4, kTileF, C::kWordRows,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  bool ok;
-  if constexpr (C::kW4)
-    ok = make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.act, a.K, a.M,
-                     static_cast<uint64_t>(a.K) * 2, 64, T, CU_TENSOR_MAP_SWIZZLE_128B);
-  else
-    ok = make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.act, a.K, a.M,
-                     static_cast<uint64_t>(a.K), 128, T, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return cudaErrorInvalidValue;
+  if (!make_map_2d(&ta, C::kW4 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   act16, a.K, a.M, static_cast<uint64_t>(a.K) * 2, 64, T,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  CUtensorMap ts;
+  if constexpr (C::kScales) {
+    if (!make_map_2d(&ts, C::kW4 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     a.scales, a.N, a.K / kGroup, static_cast<uint64_t>(a.N) * 2, kTileF, kScaleChunk,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    ts = tw;  // not read
+  }
 
-  const uint32_t fixed = 1024 + C::kBTotal + kCtrlBytes;
+  const uint32_t fixed = 1024 + C::kScaleBytes + kCtrlBytes;
   int stages = static_cast<int>((kSmemLimit - fixed) / C::kStageBytes);
   if (stages > kMaxStages) stages = kMaxStages;
   const uint32_t smem = fixed + static_cast<uint32_t>(stages) * C::kStageBytes;
@@ -612,7 +812,6 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
 
   KParams kp;
   kp.s_a = a.s_a;
-  kp.scales = a.scales;
   kp.out = a.out;
   kp.M = a.M;
   kp.N = a.N;
@@ -624,8 +823,8 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
   kp.err = err;
   kp.limit_ns = kWaitLimitNs;
   kp.stages = stages;
-  qlin_gemm_kernel<kMode, T><<<static_cast<unsigned>(pl.ctas), kThreads, smem, stream>>>(tw, ta, kp);
-  return cudaGetLastError();
+  return launch_pdl(qlin_gemm_kernel<kMode, T>, dim3(static_cast<unsigned>(pl.ctas)),
+                    dim3(kThreads), smem, stream, tw, ta, ts, kp);
 }
 
 template <int kMode>
@@ -648,10 +847,23 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
   p.TT = (M + p.T - 1) / p.T;
   p.G = K / kGroup;
   p.steps = p.TT * p.F * p.G;
-  p.ctas = p.steps < sm_count ? p.steps : sm_count;
+  // At least kMinSteps (tile, group) steps per block: small layers use fewer
+  // blocks instead of splitting every tile across many of them.
+  const int64_t by_work = (p.steps + kMinSteps - 1) / kMinSteps;
+  p.ctas = by_work < sm_count ? by_work : sm_count;
+  if (p.ctas > static_cast<int64_t>(kCounterBytes / sizeof(int)))
+    p.ctas = static_cast<int64_t>(kCounterBytes / sizeof(int));
   if (p.ctas < 1) p.ctas = 1;
-  p.counter_bytes = ((static_cast<size_t>(p.TT * p.F) * sizeof(int)) + 255) & ~static_cast<size_t>(255);
-  p.workspace_bytes = p.counter_bytes + static_cast<size_t>(p.ctas) * 2 * p.T * kTileF * sizeof(float);
+  // One arrival counter per block: a tile split across blocks is counted on
+  // the counter of its first contributing block, and a block is the first
+  // contributor of at most one split tile (the tile its range ends in).  The
+  // counters sit in a fixed region at the start of the workspace, so calls of
+  // any shape that share a workspace never see each other's partials there.
+  p.counter_bytes = kCounterBytes;
+  const size_t partial_bytes = static_cast<size_t>(p.ctas) * 2 * p.T * kTileF * sizeof(float);
+  // then the fp16 image of the W8A8 activations (1 KB aligned)
+  p.act_offset = (p.counter_bytes + partial_bytes + 1023) & ~static_cast<size_t>(1023);
+  p.workspace_bytes = p.act_offset + static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
   return p;
 }
 

@@ -148,6 +148,29 @@ __device__ __forceinline__ bool named_bar_and(int id, int threads, bool pred) {
   return r != 0;
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Blocks until the grids this one depends on (launched before it on the
+// stream with programmatic serialization) have completed and their memory is
+// visible.  A no-op when the kernel was launched without that attribute.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel on the stream (if launched with programmatic
+// serialization) start its blocks; it still waits for this grid's completion
+// before it reads what this grid writes.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// int atomic add with acquire-release semantics at GPU scope.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -51,11 +51,31 @@ struct GemmPlan {
   int64_t steps;   // TT * F * G
   int64_t ctas;    // grid size
   size_t counter_bytes;
+  size_t act_offset;     // fp16 image of the W8A8 activations in the workspace
   size_t workspace_bytes;
 };
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count);
 
 cudaError_t launch_gemm(const GemmArgs& a, const GemmPlan& p, int* err, cudaStream_t stream);
+
+// Launches `kernel` with programmatic stream serialization: it may start
+// before the previous kernel on the stream has finished, and must call
+// griddepcontrol.wait before it touches memory that kernel produces or uses.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace qlin
