@@ -55,6 +55,7 @@ typedef int qlin_status_t;
 #define QLIN_ERR_WORKSPACE       -4   /* workspace NULL or smaller than qlin_workspace_bytes() */
 #define QLIN_ERR_BITS            -5   /* bits is not 4 or 8 */
 #define QLIN_ERR_DEVICE          -6   /* the current device is not an sm_103 GPU */
+#define QLIN_ERR_TOO_LARGE       -7   /* the problem needs more scratch than the no-alloc entry holds */
 #define QLIN_ERR_CUDA           -10   /* a CUDA runtime call or kernel launch failed */
 #define QLIN_ERR_DEVICE_TIMEOUT -20   /* a bounded wait inside a kernel ran out (device error word) */
 #define QLIN_ERR_VALUE_RANGE    -21   /* the packer met a value outside the bit width (device error word) */
@@ -115,6 +116,37 @@ qlin_status_t qlin_gemm_w8a8_gs128(const int8_t *q_a, const float *s_a,
                                    int64_t M, int64_t N, int64_t K, uint16_t *y,
                                    void *workspace, size_t workspace_bytes,
                                    qlin_stream_t stream);
+
+/*
+ * W8A8 GS128 linear for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for the library's
+ * users.  Some callers cannot call cudaMalloc or hand the library a workspace
+ * -- code running inside an allocator or memory-pool callback, a plugin whose
+ * host framework owns every device allocation, or a process that must not
+ * grow its device footprint once it is serving.  This call computes exactly
+ * what qlin_gemm_w8a8_gs128 computes (same kernel, same split of K, same
+ * results) but takes its scratch from a fixed 24 MiB array compiled
+ * into the library, which every GPU that loads the library holds until the
+ * process exits.  It allocates nothing.
+ *
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current) and caches it; make that first call before any stream
+ *    capture.
+ *  - Problems whose scratch need (qlin_workspace_bytes) exceeds 24 MiB return
+ *    QLIN_ERR_TOO_LARGE; on a 152-SM GB300 every shape with M <= 96 and
+ *    K <= 50,000 fits.
+ *  - All calls share the one array, which keeps the last call's contents; the
+ *    call clears the arrival counters with cudaMemsetAsync on `stream` before
+ *    its kernel.  Calls that overlap on the GPU (other streams, unordered host
+ *    threads) race on the array: order them on one stream.
+ *
+ * Arguments as for qlin_gemm_w8a8_gs128, without the workspace.
+ */
+qlin_status_t qlin_gemm_w8a8_gs128_noalloc(const int8_t *q_a, const float *s_a,
+                                           const int32_t *qweight, const uint16_t *scales,
+                                           int64_t M, int64_t N, int64_t K, uint16_t *y,
+                                           qlin_stream_t stream);
 
 /*
  * W4A16 g128 symmetric weight-only linear:

@@ -198,6 +198,7 @@ const char* qlin_status_string(qlin_status_t status) {
     case QLIN_ERR_WORKSPACE: return "workspace is NULL or smaller than qlin_workspace_bytes()";
     case QLIN_ERR_BITS: return "bits must be 4 or 8";
     case QLIN_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    case QLIN_ERR_TOO_LARGE: return "the problem needs more scratch than the no-alloc entry's 24 MiB array";
     case QLIN_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case QLIN_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
     case QLIN_ERR_VALUE_RANGE: return "the packer met a value outside the bit width";

@@ -25,6 +25,7 @@ QLIN_ERR_ALIGN = -3
 QLIN_ERR_WORKSPACE = -4
 QLIN_ERR_BITS = -5
 QLIN_ERR_DEVICE = -6
+QLIN_ERR_TOO_LARGE = -7
 QLIN_ERR_CUDA = -10
 QLIN_ERR_DEVICE_TIMEOUT = -20
 QLIN_ERR_VALUE_RANGE = -21
@@ -32,6 +33,7 @@ QLIN_ERR_VALUE_RANGE = -21
 EXPORTS = (
     "qlin_act_quant_i8",
     "qlin_gemm_w8a8_gs128",
+    "qlin_gemm_w8a8_gs128_noalloc",
     "qlin_gemm_w4a16_g128",
     "qlin_pack_gptq",
     "qlin_workspace_bytes",
@@ -72,6 +74,7 @@ def load():
         sig = {
             "qlin_act_quant_i8": ([P, I64, I64, P, P, P], I),
             "qlin_gemm_w8a8_gs128": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_gemm_w8a8_gs128_noalloc": ([P, P, P, P, I64, I64, I64, P, P], I),
             "qlin_gemm_w4a16_g128": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_pack_gptq": ([P, I64, I64, I, P, P, P], I),
             "qlin_workspace_bytes": ([I64, I64, I64], SZ),
@@ -192,6 +195,30 @@ def gemm_w8a8_gs128(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
     ws = _workspace(workspace, M, N, K, q_a.device)
     _check(load().qlin_gemm_w8a8_gs128(_ptr(q_a), _ptr(s_a), _ptr(qweight), _ptr(scales), M, N, K,
                                        _ptr(y), _ptr(ws), ws.numel(), _stream_handle(stream)))
+    return y
+
+
+def gemm_w8a8_gs128_noalloc(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
+                            scales: torch.Tensor, y: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """W8A8 GS128 linear that allocates nothing inside the library: its split-K
+    scratch is the library's built-in 24 MiB device array (for callers that
+    cannot allocate; see include/qlin.h).  Same arguments and result as
+    gemm_w8a8_gs128 without the workspace.  Calls that overlap on the GPU
+    race on the shared array."""
+    _need(q_a, "q_a", torch.int8, 2)
+    _need(s_a, "s_a", torch.float32, 1)
+    _need(qweight, "qweight", torch.int32, 2)
+    _need(scales, "scales", torch.float16, 2)
+    M, K = q_a.shape
+    N = qweight.shape[1]
+    if qweight.shape[0] * 4 != K or scales.shape != (K // 128, N) or s_a.shape[0] != M:
+        raise ValueError("inconsistent W8A8 shapes")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=q_a.device)
+    _need(y, "y", torch.bfloat16, 2)
+    _check(load().qlin_gemm_w8a8_gs128_noalloc(_ptr(q_a), _ptr(s_a), _ptr(qweight), _ptr(scales),
+                                               M, N, K, _ptr(y), _stream_handle(stream)))
     return y
 
 
