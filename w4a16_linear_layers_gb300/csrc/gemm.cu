@@ -79,8 +79,9 @@ struct Cfg {
   static constexpr bool kW4 = kMode == kModeW4;
   // warps 0..3: control (0 weight TMA, 1 TMEM owner + MMA issuer, 2 activation
   //             and scale TMA, 3 MMA issuer)
-  // warps 4..11: converters, two groups of four (each group converts half of
-  //              every 128-wide K group; warp w serves TMEM lanes 32*(w%4)..)
+  // warps 4..11: converters, two groups of four taking alternate steps (each
+  //              converts a whole 128-wide K group; warp w serves TMEM lanes
+  //              32*(w%4)..)
   // warps 12..19: epilogue, two groups of four (each drains half of the T
   //              token columns of the accumulator)
   static constexpr int kConvWarp0 = 4;
@@ -101,13 +102,14 @@ struct Cfg {
   // A (64 TMEM columns) and, for W8A8, D (T columns) buffers in flight
   // between the converters, the MMA issuers and the epilogue.
   static constexpr int kNumBufRaw = kW4 ? (512 - kW4DCols) / 64 : 512 / (64 + T);
-  static constexpr int kNumBuf = kNumBufRaw < 4 ? kNumBufRaw : 4;
+  static constexpr int kNumBuf = kNumBufRaw < 6 ? kNumBufRaw : 6;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColA = 0;
   static constexpr uint32_t kColD = 64 * kNumBuf;
   static constexpr int kEpiCols = T / 2;                     // columns per epilogue thread
-  // a stage is released by the converters (weights) and the MMA (activations)
-  static constexpr uint32_t kEmptyCount = kConvWarps + 1;
+  // a stage is released by one converter group (weights) and the MMA
+  // (activations)
+  static constexpr uint32_t kEmptyCount = kConvWarps / 2 + 1;
   // Group scales travel by TMA into a ring of their own (kScaleChunk groups x
   // 128 x 16-bit per slot), read by the epilogue (W8A8) or the converters
   // (W4A16).
@@ -122,7 +124,7 @@ struct Cfg {
   static_assert(kConvThreads == 256 && kEpiThreads == 256, "warp roles");
 };
 
-constexpr int kBufMax = 4;
+constexpr int kBufMax = 6;
 
 struct KParams {
   const float* s_a;
@@ -137,7 +139,8 @@ struct KParams {
 
 // Shared control block (after the stage ring and the scale ring).
 struct Ctrl {
-  uint64_t full[kMaxStages];
+  uint64_t wfull[kMaxStages];   // the stage's weights landed
+  uint64_t xfull[kMaxStages];   // the stage's activations landed
   uint64_t empty[kMaxStages];
   uint64_t a_full[kBufMax];
   uint64_t a_empty[kBufMax];
@@ -228,33 +231,48 @@ __device__ __forceinline__ void int4x8_to_bf16x8(uint32_t w, uint32_t s2, uint32
 // All lanes of the warp agree on a wait's outcome.
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xFFFFFFFFu, ok); }
 
-// Finish a block's segment of a tile whose K was split across blocks: publish
-// this block's fp32 partial, count the arrival on the counter of the tile's
-// first contributing block, and if this block is the last to arrive, sum every
-// contributor's partial in ascending block order into `vals`.  Returns true
-// when `vals` now holds the whole tile's sum (this block writes the output).
+// A tile whose K was split across blocks is finished by the last of its
+// blocks to arrive.  Each block publishes its fp32 partial and counts its
+// arrival on the counter of the tile's first contributing block right away
+// (split_publish), but looks at the arrival count only after its last step
+// (split_finish), so no block stalls mid-stream on the atomic's round trip.
 // Ordering: the epilogue threads' partial stores are ordered before thread 0's
-// release by the barrier; the acquire half of the same atomic, followed by
-// the barrier, orders the last block's reads after every contributor's stores.
+// release by the barrier; the acquire half of the same atomic, followed by a
+// barrier, orders the last block's reads after every contributor's stores.
+struct PendingSplit {
+  int64_t tile = -1;
+  int old = 0;       // arrivals before this block's (thread 0 only)
+};
+
 template <int kCols>
-__device__ __forceinline__ bool split_tile_fixup(const KParams& p, Ctrl* ctrl, int64_t tile,
-                                                 int64_t cta, int64_t nC, int64_t first_tile,
-                                                 int colbase, int r, int et, int epi_threads,
-                                                 float* vals) {
-  const int64_t G = p.G;
+__device__ __forceinline__ void split_publish(const KParams& p, int64_t tile, int64_t cta,
+                                              int64_t nC, int64_t first_tile, int colbase, int r,
+                                              int et, int epi_threads, const float* vals,
+                                              PendingSplit& pend) {
   const int slot = (tile == first_tile) ? 0 : 1;
   float* mine = p.part + ((cta * 2 + slot) * (2 * kCols)) * kTileF;
 #pragma unroll
   for (int c = 0; c < kCols; ++c) mine[(colbase + c) * kTileF + r] = vals[c];
   named_bar_sync(1, epi_threads);
+  pend.tile = tile;
+  if (et == 0) pend.old = atomic_add_acq_rel_gpu(&p.counters[cta_of_step(tile * p.G, nC, p.W)], 1);
+}
+
+// Returns true when this block arrived last; `vals` then holds the tile's sum
+// over all contributors in ascending block order.
+template <int kCols>
+__device__ __forceinline__ bool split_finish(const KParams& p, Ctrl* ctrl, const PendingSplit& pend,
+                                             int64_t nC, int colbase, int r, int et,
+                                             int epi_threads, float* vals) {
+  const int64_t G = p.G;
+  const int64_t tile = pend.tile;
   const int64_t c_first = cta_of_step(tile * G, nC, p.W);
   const int64_t c_last = cta_of_step(tile * G + G - 1, nC, p.W);
-  if (et == 0) {
-    const int old = atomic_add_acq_rel_gpu(&p.counters[c_first], 1);
-    ctrl->last_flag = (old == static_cast<int>(c_last - c_first)) ? 1 : 0;
-  }
+  if (et == 0) ctrl->last_flag = (pend.old == static_cast<int>(c_last - c_first)) ? 1 : 0;
   named_bar_sync(1, epi_threads);
-  if (!ctrl->last_flag) return false;
+  const bool last = ctrl->last_flag != 0;
+  named_bar_sync(1, epi_threads);     // last_flag may be rewritten by the next call
+  if (!last) return false;
   // Sum in ascending contributor order; loads of several contributors are in
   // flight at once (8 columns at a time) to hide the L2 round trips.
   auto part_of = [&](int64_t cc) {
@@ -326,11 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
-      mbar_init(smem_u32(&ctrl->full[i]), 2);      // weight producer + activation producer
+      mbar_init(smem_u32(&ctrl->wfull[i]), 1);
+      mbar_init(smem_u32(&ctrl->xfull[i]), 1);
       mbar_init(smem_u32(&ctrl->empty[i]), C::kEmptyCount);
     }
     for (int i = 0; i < NB; ++i) {
-      mbar_init(smem_u32(&ctrl->a_full[i]), C::kConvWarps);
+      mbar_init(smem_u32(&ctrl->a_full[i]), C::kConvWarps / 2);
       mbar_init(smem_u32(&ctrl->a_empty[i]), 1);
       mbar_init(smem_u32(&ctrl->d_full[i]), C::kW4 ? C::kIssuers : 1);
       mbar_init(smem_u32(&ctrl->d_empty[i]), C::kEpiWarps);
@@ -349,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     StepIter it(s0, G, F);
     const int first = n_steps < stages ? n_steps : stages;
     for (int j = 0; j < first; ++j, it.next()) {
-      const uint32_t full = smem_u32(&ctrl->full[j]);
+      const uint32_t full = smem_u32(&ctrl->wfull[j]);
       mbar_arrive_expect_tx(full, C::kWBytes);
       tma_load_2d(sbase + static_cast<uint32_t>(j) * C::kStageBytes, &tm_w, full,
                   static_cast<int32_t>(it.f * kTileF), static_cast<int32_t>(it.g * C::kWordRows),
@@ -382,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int j = w_issued; j < n_steps; ++j, it.next(), rg.next()) {
         if (!mbar_wait(smem_u32(&ctrl->empty[rg.slot]), rg.phase ^ 1u, ctx, 1)) break;
-        const uint32_t full = smem_u32(&ctrl->full[rg.slot]);
+        const uint32_t full = smem_u32(&ctrl->wfull[rg.slot]);
         mbar_arrive_expect_tx(full, C::kWBytes);
         tma_load_2d(sbase + static_cast<uint32_t>(rg.slot) * C::kStageBytes, &tm_w, full,
                     static_cast<int32_t>(it.f * kTileF), static_cast<int32_t>(it.g * C::kWordRows),
@@ -391,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every load issued must land before the block exits.
       for (int j = w_issued > stages ? w_issued - stages : 0; j < w_issued; ++j)
-        (void)mbar_wait(smem_u32(&ctrl->full[j % stages]),
+        (void)mbar_wait(smem_u32(&ctrl->wfull[j % stages]),
                         static_cast<uint32_t>(j / stages) & 1u, drain_ctx, 2);
     }
     __syncwarp();
@@ -424,17 +443,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           grid_dep_wait();   // the activations come from the previous kernel
           waited = true;
         }
-        const uint32_t full = smem_u32(&ctrl->full[rg.slot]);
+        const uint32_t full = smem_u32(&ctrl->xfull[rg.slot]);
         const uint32_t dst = sbase + static_cast<uint32_t>(rg.slot) * C::kStageBytes + C::kWBytes;
         mbar_arrive_expect_tx(full, C::kABytes);
-        tma_load_2d(dst, &tm_a, full, static_cast<int32_t>(it.g * kGroup),
-                    static_cast<int32_t>(it.t * T), pol_a);
-        tma_load_2d(dst + T * 128u, &tm_a, full, static_cast<int32_t>(it.g * kGroup + 64),
-                    static_cast<int32_t>(it.t * T), pol_a);
+        // one load brings both 64-wide halves of the group, each as a T x 128 B
+        // swizzled tile (the activations seen as [K/64 halves][M rows][64])
+        tma_load_3d(dst, &tm_a, full, 0, static_cast<int32_t>(it.t * T),
+                    static_cast<int32_t>(it.g * 2), pol_a);
         ++issued;
       }
       for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
-        (void)mbar_wait(smem_u32(&ctrl->full[j % stages]),
+        (void)mbar_wait(smem_u32(&ctrl->xfull[j % stages]),
                         static_cast<uint32_t>(j / stages) & 1u, drain_ctx, 16);
       for (int c = s_issued > SR ? s_issued - SR : 0; c < s_issued; ++c)
         (void)mbar_wait(smem_u32(&ctrl->s_full[c % SR]), static_cast<uint32_t>(c / SR) & 1u,
@@ -463,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : tmem + C::kColD + ab * T;
         if ((j & 1) == me) {
           const bool need_d = C::kW4 ? !started : true;
-          if (!mbar_wait(smem_u32(&ctrl->full[rg.slot]), rg.phase, ctx, 3)) break;
+          if (!mbar_wait(smem_u32(&ctrl->xfull[rg.slot]), rg.phase, ctx, 3)) break;
           if (!mbar_wait(smem_u32(&ctrl->a_full[ab]), abph, ctx, 4)) break;
           if (need_d && !mbar_wait(smem_u32(&ctrl->d_empty[db]), dbph ^ 1u, ctx, 5)) break;
           tc_fence_after();
@@ -508,60 +527,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= C::kConvWarp0 && warp < C::kEpiWarp0) {
     // ------------------------------------------------------------ converters
+    // group 0 (warps 4-7) takes the even steps, group 1 (warps 8-11) the odd
+    // ones, so one group's load/convert/store latency overlaps the other's
     const int ct = threadIdx.x - 32 * C::kConvWarp0;      // 0..255
-    const int kh = ct >> 7;                                // half of the group's K
+    const int grp = ct >> 7;
     const int r = ct & 127;                                // row of A = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     StepIter it(s0, G, F);
     Ring rg(stages);
     ChunkIter ch;
+    bool chunk_ready = false;   // W4A16: this group has waited for the chunk's scales
     for (int j = 0; j < n_steps; ++j, it.next(), rg.next(), ch.advance()) {
-      const int ab = j % NB;
-      const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
-      bool ok = mbar_wait(smem_u32(&ctrl->full[rg.slot]), rg.phase, ctx, 7);
-      if (ok) ok = mbar_wait(smem_u32(&ctrl->a_empty[ab]), abph ^ 1u, ctx, 8);
-      uint32_t s2 = 0;
+      const bool seg_last = (j == n_steps - 1) || (it.g == G - 1);
       if constexpr (C::kW4) {
-        const bool seg_last = (j == n_steps - 1) || (it.g == G - 1);
-        ch.begin(j == 0 || it.g == 0);
-        const int slot = ch.ci % SR;
-        if (ok && ch.row() == 0)
-          ok = mbar_wait(smem_u32(&ctrl->s_full[slot]), static_cast<uint32_t>(ch.ci / SR) & 1u,
-                         ctx, 13);
-        if (!warp_all(ok)) break;
-        const uint32_t sb = scale_ring[(slot * kScaleChunk + ch.row()) * 128 + r];
-        s2 = sb | (sb << 16);
+        if (ch.begin(j == 0 || it.g == 0)) chunk_ready = false;
+      }
+      const bool mine = (j & 1) == grp;
+      if (mine) {
+        const int ab = j % NB;
+        const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
+        bool ok = mbar_wait(smem_u32(&ctrl->wfull[rg.slot]), rg.phase, ctx, 7);
+        if (ok) ok = mbar_wait(smem_u32(&ctrl->a_empty[ab]), abph ^ 1u, ctx, 8);
+        uint32_t s2 = 0;
+        if constexpr (C::kW4) {
+          const int slot = ch.ci % SR;
+          if (ok && !chunk_ready)
+            ok = mbar_wait(smem_u32(&ctrl->s_full[slot]), static_cast<uint32_t>(ch.ci / SR) & 1u,
+                           ctx, 13);
+          if (!warp_all(ok)) break;
+          chunk_ready = true;
+          const uint32_t sb = scale_ring[(slot * kScaleChunk + ch.row()) * 128 + r];
+          s2 = sb | (sb << 16);
+        } else {
+          if (!warp_all(ok)) break;
+        }
+        tc_fence_after();
+        const uint32_t* wsm = reinterpret_cast<const uint32_t*>(
+            smem + static_cast<uint32_t>(rg.slot) * C::kStageBytes);
+        const uint32_t acol = tmem + lane_off + C::kColA + ab * 64;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t v[16];
+          if constexpr (C::kW4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              int4x8_to_bf16x8(wsm[(h * 4 + i) * kTileF + r], s2, v + 4 * i);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              biased_u8x4_to_f16x4(wsm[(h * 8 + i) * kTileF + r], v[2 * i], v[2 * i + 1]);
+          }
+          tmem_st16(acol + h * 16, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&ctrl->empty[rg.slot]));
+          mbar_arrive(smem_u32(&ctrl->a_full[ab]));
+        }
+      }
+      if constexpr (C::kW4) {
+        // both groups release each scale chunk (a group that had no step in it
+        // read nothing from it)
         if (ch.ends(seg_last)) {
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctrl->s_empty[slot]));
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->s_empty[ch.ci % SR]));
         }
-      } else {
-        if (!warp_all(ok)) break;
-      }
-      tc_fence_after();
-      const uint32_t* wsm =
-          reinterpret_cast<const uint32_t*>(smem + static_cast<uint32_t>(rg.slot) * C::kStageBytes);
-      const uint32_t acol = tmem + lane_off + C::kColA + ab * 64 + kh * 32;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[16];
-        if constexpr (C::kW4) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            int4x8_to_bf16x8(wsm[(kh * 8 + h * 4 + i) * kTileF + r], s2, v + 4 * i);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            biased_u8x4_to_f16x4(wsm[(kh * 16 + h * 8 + i) * kTileF + r], v[2 * i], v[2 * i + 1]);
-        }
-        tmem_st16(acol + h * 16, v);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&ctrl->empty[rg.slot]));
-        mbar_arrive(smem_u32(&ctrl->a_full[ab]));
       }
     }
     __syncwarp();
@@ -581,6 +613,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int seg = 0;
     int seg_j0 = 0;             // first step of the current segment
     bool waited = false;
+    PendingSplit pend[2];       // at most the first and the last tile of the range
+    int npend = 0;
+    auto write_out = [&](int64_t tt, int64_t nn, const float* vals) {
+      if (nn >= N) return;
+#pragma unroll
+      for (int c = 0; c < C::kEpiCols; ++c) {
+        const int64_t m = tt * T + colbase + c;
+        if (m < M) {
+          const float v = C::kW4 ? vals[c] : vals[c] * __ldg(p.s_a + m);
+          y[m * N + nn] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        }
+      }
+    };
     StepIter it(s0, G, F);
     ChunkIter ch;
     for (int j = 0; j < n_steps; ++j, it.next(), ch.advance()) {
@@ -677,18 +722,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int64_t tile = it.tile();
       const bool full_tile = (seg_g0 == 0) && (g == G - 1);
-      bool write = full_tile;
-      if (!full_tile)
-        write = split_tile_fixup<C::kEpiCols>(p, ctrl, tile, cta, nC, first_tile, colbase, r, et,
-                                              C::kEpiThreads, acc);
-      if (write && n < N) {
-#pragma unroll
-        for (int c = 0; c < C::kEpiCols; ++c) {
-          const int64_t m = t * T + colbase + c;
-          if (m < M) {
-            const float v = C::kW4 ? acc[c] : acc[c] * __ldg(p.s_a + m);
-            y[m * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-          }
+      if (full_tile) {
+        write_out(t, n, acc);
+      } else {
+        split_publish<C::kEpiCols>(p, tile, cta, nC, first_tile, colbase, r, et, C::kEpiThreads,
+                                   acc, pend[npend]);
+        ++npend;
+      }
+    }
+    // the split tiles this block took part in: the last block to arrive sums
+    // the partials and writes the output
+    if (named_bar_and(2, C::kEpiThreads, alive)) {
+      for (int k = 0; k < npend; ++k) {
+        if (split_finish<C::kEpiCols>(p, ctrl, pend[k], nC, colbase, r, et, C::kEpiThreads, acc)) {
+          const int64_t tt = pend[k].tile / F;
+          write_out(tt, (pend[k].tile - tt * F) * kTileF + r, acc);
         }
       }
     }
@@ -743,6 +791,22 @@ EncodeFn encode_fn() {
   return fn;
 }
 
+// 16-bit activations [M][K] seen as a 3D tensor {64 (k inside a half group),
+// M (rows, stride K*2 bytes), K/64 (half groups, stride 128 bytes)}; a box
+// {64, T, 2} is one 128-wide K group as two swizzled T x 128 B tiles.
+bool make_act_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t M,
+                  uint64_t K, uint32_t T) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {64, M, K / 64};
+  const cuuint64_t strides[2] = {K * 2, 128};
+  const cuuint32_t box[3] = {64, T, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                  CUtensorMapSwizzle swz) {
@@ -782,9 +846,8 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
                    static_cast<uint64_t>(a.N) * 4, kTileF, C::kWordRows,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (!make_map_2d(&ta, C::kW4 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                   act16, a.K, a.M, static_cast<uint64_t>(a.K) * 2, 64, T,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_act_map(&ta, C::kW4 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    act16, a.M, a.K, T))
     return cudaErrorInvalidValue;
   CUtensorMap ts;
   if constexpr (C::kScales) {
