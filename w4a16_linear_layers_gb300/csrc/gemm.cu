@@ -65,10 +65,12 @@ constexpr int kThreads = 640;
 constexpr int kTileF = 128;            // features per tile = MMA M
 constexpr uint32_t kSmemLimit = 232448; // 227 KB opt-in shared memory per block
 constexpr uint32_t kCtrlBytes = 1024;
-constexpr int kMaxStages = 10;
+constexpr int kMaxStages = 16;           // weight ring slots
+constexpr int kMaxXSlots = 16;           // activation ring slots
 constexpr size_t kCounterBytes = 4096;   // int counters for up to 1024 blocks
 constexpr int64_t kMinSteps = 8;          // minimum (tile, group) steps per block
 constexpr int kScaleChunk = 8;            // groups of scales per TMA load
+constexpr int kPreW = 3;                  // weight loads issued before the first activations
 
 constexpr int kModeW8A8 = 0;
 constexpr int kModeP = 1;     // W8A8 pipeline, exports the group partials
@@ -93,7 +95,14 @@ struct Cfg {
   static constexpr int kWordRows = kW4 ? 16 : 32;           // int32 rows per group
   static constexpr uint32_t kWBytes = kWordRows * kTileF * 4;
   static constexpr uint32_t kABytes = 2u * T * 128u;         // two 64-wide 16-bit halves
-  static constexpr uint32_t kStageBytes = (kWBytes + kABytes + 1023u) & ~1023u;
+  // Weights and activations travel in rings of their own: a weight slot is
+  // freed as soon as the converters have moved it into TMEM, an activation
+  // slot when the MMAs that read it have completed, so neither stream waits
+  // for the other's consumer.  The activation ring is deep enough to cover
+  // the L2 latency seen while the weight stream keeps HBM busy.
+  static constexpr uint32_t kStageBytes = kWBytes;
+  static constexpr int kXSlotsRaw = static_cast<int>(65536u / kABytes);
+  static constexpr int kXSlotsW4 = kXSlotsRaw < 4 ? 4 : (kXSlotsRaw > kMaxXSlots ? kMaxXSlots : kXSlotsRaw);
   static constexpr int kIssuers = 2;
   // W4A16 accumulates a whole segment in TMEM: one accumulator per issuer
   // and segment buffer (two segment buffers while they fit).
@@ -101,15 +110,30 @@ struct Cfg {
   static constexpr int kW4DCols = kW4 ? kSegBufs * kIssuers * T : 0;
   // A (64 TMEM columns) and, for W8A8, D (T columns) buffers in flight
   // between the converters, the MMA issuers and the epilogue.
-  static constexpr int kNumBufRaw = kW4 ? (512 - kW4DCols) / 64 : 512 / (64 + T);
+  // W8A8 sizes the A buffers (converter -> MMA) and the D buffers (MMA ->
+  // epilogue) separately: the epilogue loop (MMA completion, TMEM drain,
+  // release) is the long one, so small token tiles get many D buffers.
+  static constexpr int kNumBufRaw = kW4 ? (512 - kW4DCols) / 64 : (T <= 64 ? 4 : 2);
   static constexpr int kNumBuf = kNumBufRaw < 6 ? kNumBufRaw : 6;
+  static constexpr int kNumDFit = kW4 ? 1 : (512 - 64 * kNumBuf) / T;
+  static constexpr int kNumDRaw = kNumDFit < 16 ? kNumDFit : 16;
+  // ND - NA even: see the waits of the converters
+  static constexpr int kNumD = kW4 ? 1 : kNumDRaw - ((kNumDRaw - kNumBuf) & 1);
+  // W8A8 commits once per step, on the step's D buffer: that completion also
+  // frees the step's A buffer and activation slot.  The activation ring then
+  // has one slot per D buffer, so a slot's producer waits for the completion
+  // of the step that last used it, which is always the D buffer's latest
+  // phase (the buffer's next phase needs the very slot being refilled).
+  static constexpr int kXSlots = kW4 ? kXSlotsW4 : kNumD;
+  static_assert(kW4 || (kNumD >= kNumBuf && (kNumD - kNumBuf) % 2 == 0),
+                "one commit per step needs ND >= NA with ND - NA even");
+  static_assert(kW4 || kXSlots == kNumD, "activation slot i pairs with D buffer i");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColA = 0;
   static constexpr uint32_t kColD = 64 * kNumBuf;
   static constexpr int kEpiCols = T / 2;                     // columns per epilogue thread
-  // a stage is released by one converter group (weights) and the MMA
-  // (activations)
-  static constexpr uint32_t kEmptyCount = kConvWarps / 2 + 1;
+  // a weight slot is released by the four warps of one converter group
+  static constexpr uint32_t kEmptyCount = kConvWarps / 2;
   // Group scales travel by TMA into a ring of their own (kScaleChunk groups x
   // 128 x 16-bit per slot), read by the epilogue (W8A8) or the converters
   // (W4A16).
@@ -120,11 +144,13 @@ struct Cfg {
   static_assert(T % 16 == 0 && T >= 16 && T <= 128, "token tile");
   static_assert(kEpiCols % 8 == 0, "epilogue columns");
   static_assert(kNumBuf >= 2, "double buffering at least");
-  static_assert(kColD + (kW4 ? kW4DCols : kNumBuf * T) <= kTmemCols, "TMEM budget");
+  static_assert(kColD + (kW4 ? kW4DCols : kNumD * T) <= kTmemCols, "TMEM budget");
+  static_assert(kW4 || kNumD >= 2, "double buffering at least");
   static_assert(kConvThreads == 256 && kEpiThreads == 256, "warp roles");
 };
 
-constexpr int kBufMax = 6;
+constexpr int kBufMax = 6;     // A buffers
+constexpr int kDBufMax = 16;   // D buffers
 
 struct KParams {
   const float* s_a;
@@ -139,20 +165,25 @@ struct KParams {
 
 // Shared control block (after the stage ring and the scale ring).
 struct Ctrl {
-  uint64_t wfull[kMaxStages];   // the stage's weights landed
-  uint64_t xfull[kMaxStages];   // the stage's activations landed
-  uint64_t empty[kMaxStages];
+  uint64_t wfull[kMaxStages];   // the slot's weights landed
+  uint64_t empty[kMaxStages];   // the slot's weights are in TMEM
+  uint64_t xfull[kMaxXSlots];   // the slot's activations landed
+  uint64_t xempty[kMaxXSlots];  // the MMAs reading the slot completed
   uint64_t a_full[kBufMax];
   uint64_t a_empty[kBufMax];
-  uint64_t d_full[kBufMax];
-  uint64_t d_empty[kBufMax];
+  uint64_t d_full[kDBufMax];
+  uint64_t d_empty[kDBufMax];
   uint64_t s_full[4];
   uint64_t s_empty[4];
   uint64_t mma_done;
+  uint64_t x_go;                // the first activation loads are queued
+  uint64_t fix_full;            // split-tile partials landed in shared memory
   uint32_t tmem_base;
   int abort_flag;
   int last_flag;
 };
+
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 __device__ __forceinline__ int64_t cta_of_step(int64_t s, int64_t C, int64_t W) {
   return ((s + 1) * C + W - 1) / W - 1;
@@ -259,11 +290,16 @@ __device__ __forceinline__ void split_publish(const KParams& p, int64_t tile, in
 }
 
 // Returns true when this block arrived last; `vals` then holds the tile's sum
-// over all contributors in ascending block order.
+// over all contributors in ascending block order.  Each contributor's partial
+// (T x 128 fp32, contiguous) comes into shared memory with one bulk copy, as
+// many at a time as the idle weight and activation rings hold, so the sum
+// costs one L2 round trip per batch instead of one per column chunk.
 template <int kCols>
 __device__ __forceinline__ bool split_finish(const KParams& p, Ctrl* ctrl, const PendingSplit& pend,
                                              int64_t nC, int colbase, int r, int et,
-                                             int epi_threads, float* vals) {
+                                             int epi_threads, float* vals, uint32_t stage_addr,
+                                             const float* stage, uint32_t stage_bytes,
+                                             uint32_t& fix_phase, const WaitCtx& ctx) {
   const int64_t G = p.G;
   const int64_t tile = pend.tile;
   const int64_t c_first = cta_of_step(tile * G, nC, p.W);
@@ -273,40 +309,37 @@ __device__ __forceinline__ bool split_finish(const KParams& p, Ctrl* ctrl, const
   const bool last = ctrl->last_flag != 0;
   named_bar_sync(1, epi_threads);     // last_flag may be rewritten by the next call
   if (!last) return false;
-  // Sum in ascending contributor order; loads of several contributors are in
-  // flight at once (8 columns at a time) to hide the L2 round trips.
-  auto part_of = [&](int64_t cc) {
-    const int slot2 = ((cc * p.W / nC) / G == tile) ? 0 : 1;
-    return p.part + ((cc * 2 + slot2) * (2 * kCols)) * kTileF + static_cast<int64_t>(colbase) * kTileF + r;
-  };
-  constexpr int kC8 = kCols < 8 ? kCols : 8;
-  constexpr int kU = kCols <= 16 ? 4 : 2;     // contributors in flight
+  constexpr uint32_t kPartBytes = 2u * kCols * kTileF * sizeof(float);
+  const int64_t cap = static_cast<int64_t>(stage_bytes / kPartBytes);
 #pragma unroll
-  for (int c0 = 0; c0 < kCols; c0 += kC8) {
-    float sum[kC8];
-#pragma unroll
-    for (int c = 0; c < kC8; ++c) sum[c] = 0.0f;
-    int64_t cc = c_first;
-    for (; cc + kU - 1 <= c_last; cc += kU) {
-      float v[kU][kC8];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const float* pp = part_of(cc + u);
-#pragma unroll
-        for (int c = 0; c < kC8; ++c) v[u][c] = __ldcg(pp + (c0 + c) * kTileF);
+  for (int c = 0; c < kCols; ++c) vals[c] = 0.0f;
+  bool ok = true;
+  for (int64_t b0 = c_first; b0 <= c_last; b0 += cap) {
+    const int64_t nb = (c_last - b0 + 1) < cap ? (c_last - b0 + 1) : cap;
+    if (et == 0) {
+      // the rings were last touched by generic loads and stores (converters,
+      // the previous batch's sums): order those before the async copies
+      fence_proxy_async_smem();
+      const uint32_t full = smem_u32(&ctrl->fix_full);
+      mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb) * kPartBytes);
+      for (int64_t i = 0; i < nb; ++i) {
+        const int64_t cc = b0 + i;
+        const int slot = ((cc * p.W / nC) / G == tile) ? 0 : 1;
+        bulk_load(stage_addr + static_cast<uint32_t>(i) * kPartBytes,
+                  p.part + ((cc * 2 + slot) * (2 * kCols)) * kTileF, kPartBytes, full);
       }
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-#pragma unroll
-        for (int c = 0; c < kC8; ++c) sum[c] += v[u][c];
     }
-    for (; cc <= c_last; ++cc) {
-      const float* pp = part_of(cc);
+    ok = warp_all(mbar_wait(smem_u32(&ctrl->fix_full), fix_phase, ctx, 18));
+    fix_phase ^= 1u;
+    if (ok) {
+      for (int64_t i = 0; i < nb; ++i) {
+        const float* src = stage + i * (kPartBytes / sizeof(float)) + colbase * kTileF + r;
 #pragma unroll
-      for (int c = 0; c < kC8; ++c) sum[c] += __ldcg(pp + (c0 + c) * kTileF);
+        for (int c = 0; c < kCols; ++c) vals[c] += src[c * kTileF];
+      }
     }
-#pragma unroll
-    for (int c = 0; c < kC8; ++c) vals[c0 + c] = sum[c];
+    named_bar_sync(1, epi_threads);   // the next batch overwrites the staging area
+    if (!ok) return false;
   }
   if (et == 0) p.counters[c_first] = 0;
   return true;
@@ -319,13 +352,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_s, const KParams p) {
   using C = Cfg<kMode, T>;
   constexpr int NB = C::kNumBuf;
+  constexpr int ND = C::kW4 ? C::kSegBufs : C::kNumD;
   constexpr int SR = C::kScaleSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const int stages = p.stages;
-  const uint32_t sc_off = static_cast<uint32_t>(stages) * C::kStageBytes;
+  constexpr int NX = C::kXSlots;
+  const uint32_t x_off = static_cast<uint32_t>(stages) * C::kStageBytes;
+  const uint32_t sc_off = x_off + static_cast<uint32_t>(NX) * C::kABytes;
   const uint16_t* scale_ring = reinterpret_cast<const uint16_t*>(smem + sc_off);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + sc_off + C::kScaleBytes);
 
@@ -345,12 +381,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(smem_u32(&ctrl->wfull[i]), 1);
-      mbar_init(smem_u32(&ctrl->xfull[i]), 1);
       mbar_init(smem_u32(&ctrl->empty[i]), C::kEmptyCount);
+    }
+    for (int i = 0; i < NX; ++i) {
+      mbar_init(smem_u32(&ctrl->xfull[i]), 1);
+      mbar_init(smem_u32(&ctrl->xempty[i]), 1);
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(smem_u32(&ctrl->a_full[i]), C::kConvWarps / 2);
       mbar_init(smem_u32(&ctrl->a_empty[i]), 1);
+    }
+    for (int i = 0; i < ND; ++i) {
       mbar_init(smem_u32(&ctrl->d_full[i]), C::kW4 ? C::kIssuers : 1);
       mbar_init(smem_u32(&ctrl->d_empty[i]), C::kEpiWarps);
     }
@@ -359,14 +400,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->s_empty[i]), 8);
     }
     mbar_init(smem_u32(&ctrl->mma_done), C::kIssuers);
+    mbar_init(smem_u32(&ctrl->x_go), 1);
+    mbar_init(smem_u32(&ctrl->fix_full), 1);
     ctrl->abort_flag = 0;
     ctrl->last_flag = 0;
     fence_barrier_init();
     // The weights depend on nothing: start streaming them before the block's
-    // set-up barrier (every stage is free, so no wait is needed).
+    // set-up barrier (every slot is free, so no wait is needed).  Only a few:
+    // every TMA load of the SM queues behind the ones issued before it, and
+    // the first activation tiles must not wait behind a full weight ring.
     prefetch_tmap(&tm_w);
     StepIter it(s0, G, F);
-    const int first = n_steps < stages ? n_steps : stages;
+    const int pre = kPreW < stages ? kPreW : stages;
+    const int first = n_steps < pre ? n_steps : pre;
     for (int j = 0; j < first; ++j, it.next()) {
       const uint32_t full = smem_u32(&ctrl->wfull[j]);
       mbar_arrive_expect_tx(full, C::kWBytes);
@@ -399,7 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         it.next();
         rg.next();
       }
+      const int first_w = w_issued;
       for (int j = w_issued; j < n_steps; ++j, it.next(), rg.next()) {
+        if (j == first_w && !mbar_wait(smem_u32(&ctrl->x_go), 0u, ctx, 19)) break;
         if (!mbar_wait(smem_u32(&ctrl->empty[rg.slot]), rg.phase ^ 1u, ctx, 1)) break;
         const uint32_t full = smem_u32(&ctrl->wfull[rg.slot]);
         mbar_arrive_expect_tx(full, C::kWBytes);
@@ -420,10 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_a);
       if constexpr (C::kScales) prefetch_tmap(&tm_s);
       StepIter it(s0, G, F);
-      Ring rg(stages);
+      Ring rg(NX);
       ChunkIter ch;
       int issued = 0, s_issued = 0;
       bool waited = false;
+      const int x_first = n_steps < NX ? n_steps : NX;   // loads before the weights resume
+      bool go = false;
       for (int j = 0; j < n_steps; ++j, it.next(), rg.next(), ch.advance()) {
         if constexpr (C::kScales) {
           if (ch.begin(j == 0 || it.g == 0)) {
@@ -438,23 +488,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++s_issued;
           }
         }
-        if (!mbar_wait(smem_u32(&ctrl->empty[rg.slot]), rg.phase ^ 1u, ctx, 15)) break;
+        if constexpr (C::kW4) {
+          if (!mbar_wait(smem_u32(&ctrl->xempty[rg.slot]), rg.phase ^ 1u, ctx, 15)) break;
+        } else if (j >= NX) {
+          // the slot's previous step (j - NX) used D buffer j % ND (NX == ND)
+          if (!mbar_wait(smem_u32(&ctrl->d_full[rg.slot]), rg.phase ^ 1u, ctx, 15)) break;
+        }
         if (!waited) {
           grid_dep_wait();   // the activations come from the previous kernel
           waited = true;
         }
         const uint32_t full = smem_u32(&ctrl->xfull[rg.slot]);
-        const uint32_t dst = sbase + static_cast<uint32_t>(rg.slot) * C::kStageBytes + C::kWBytes;
+        const uint32_t dst = sbase + x_off + static_cast<uint32_t>(rg.slot) * C::kABytes;
         mbar_arrive_expect_tx(full, C::kABytes);
         // one load brings both 64-wide halves of the group, each as a T x 128 B
         // swizzled tile (the activations seen as [K/64 halves][M rows][64])
         tma_load_3d(dst, &tm_a, full, 0, static_cast<int32_t>(it.t * T),
                     static_cast<int32_t>(it.g * 2), pol_a);
         ++issued;
+        if (issued == x_first) {
+          mbar_arrive(smem_u32(&ctrl->x_go));
+          go = true;
+        }
       }
-      for (int j = issued > stages ? issued - stages : 0; j < issued; ++j)
-        (void)mbar_wait(smem_u32(&ctrl->xfull[j % stages]),
-                        static_cast<uint32_t>(j / stages) & 1u, drain_ctx, 16);
+      if (!go) mbar_arrive(smem_u32(&ctrl->x_go));
+      for (int j = issued > NX ? issued - NX : 0; j < issued; ++j)
+        (void)mbar_wait(smem_u32(&ctrl->xfull[j % NX]), static_cast<uint32_t>(j / NX) & 1u,
+                        drain_ctx, 16);
       for (int c = s_issued > SR ? s_issued - SR : 0; c < s_issued; ++c)
         (void)mbar_wait(smem_u32(&ctrl->s_full[c % SR]), static_cast<uint32_t>(c / SR) & 1u,
                         drain_ctx, 12);
@@ -467,27 +527,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int me = warp == 1 ? 0 : 1;
       constexpr uint32_t idesc = idesc_f16(kTileF, T, C::kW4);
       StepIter it(s0, G, F);
-      Ring rg(stages);
+      Ring rx(NX);
       int seg = 0;
       bool started = false;   // W4A16: this issuer has accumulated into the segment
-      for (int j = 0; j < n_steps; ++j, it.next(), rg.next()) {
+      for (int j = 0; j < n_steps; ++j, it.next(), rx.next()) {
         const bool seg_first = (j == 0) || (it.g == 0);
         const bool seg_last = (j == n_steps - 1) || (it.g == G - 1);
         const int ab = j % NB;
         const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
         if (seg_first) started = false;
-        const int db = C::kW4 ? seg % C::kSegBufs : ab;
-        const uint32_t dbph = C::kW4 ? (static_cast<uint32_t>(seg / C::kSegBufs) & 1u) : abph;
+        const int didx = C::kW4 ? seg : j;
+        const int db = didx % ND;
+        const uint32_t dbph = static_cast<uint32_t>(didx / ND) & 1u;
         const uint32_t dcol = C::kW4 ? tmem + C::kColD + (db * C::kIssuers + me) * T
-                                     : tmem + C::kColD + ab * T;
+                                     : tmem + C::kColD + db * T;
         if ((j & 1) == me) {
           const bool need_d = C::kW4 ? !started : true;
-          if (!mbar_wait(smem_u32(&ctrl->xfull[rg.slot]), rg.phase, ctx, 3)) break;
+          if (!mbar_wait(smem_u32(&ctrl->xfull[rx.slot]), rx.phase, ctx, 3)) break;
           if (!mbar_wait(smem_u32(&ctrl->a_full[ab]), abph, ctx, 4)) break;
           if (need_d && !mbar_wait(smem_u32(&ctrl->d_empty[db]), dbph ^ 1u, ctx, 5)) break;
           tc_fence_after();
-          const uint32_t xb =
-              sbase + static_cast<uint32_t>(rg.slot) * C::kStageBytes + C::kWBytes;
+          const uint32_t xb = sbase + x_off + static_cast<uint32_t>(rx.slot) * C::kABytes;
           const uint64_t d0 = smem_desc(xb, 16u, 1024u, 2u);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
@@ -500,9 +560,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(dcol, tmem + C::kColA + ab * 64 + ks * 8, d0 + (off >> 4), idesc,
                    acc ? 1u : 0u);
           }
-          tc_commit(smem_u32(&ctrl->a_empty[ab]));
-          tc_commit(smem_u32(&ctrl->empty[rg.slot]));
-          if constexpr (!C::kW4) tc_commit(smem_u32(&ctrl->d_full[ab]));
+          if constexpr (C::kW4) {
+            tc_commit(smem_u32(&ctrl->a_empty[ab]));
+            tc_commit(smem_u32(&ctrl->xempty[rx.slot]));
+          } else {
+            tc_commit(smem_u32(&ctrl->d_full[db]));   // also frees A buffer and X slot
+          }
           started = true;
         }
         if constexpr (C::kW4) {
@@ -547,7 +610,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ab = j % NB;
         const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
         bool ok = mbar_wait(smem_u32(&ctrl->wfull[rg.slot]), rg.phase, ctx, 7);
-        if (ok) ok = mbar_wait(smem_u32(&ctrl->a_empty[ab]), abph ^ 1u, ctx, 8);
+        if constexpr (C::kW4) {
+          if (ok) ok = mbar_wait(smem_u32(&ctrl->a_empty[ab]), abph ^ 1u, ctx, 8);
+        } else if (ok && j >= NB) {
+          // A buffer ab was last read by step j - NB, committed on its D
+          // buffer.  That buffer's next completion is step j - NB + ND, which
+          // (ND - NB even) belongs to this converter group and so comes after
+          // this conversion: the parity below cannot be overtaken.
+          const int pj = j - NB;
+          ok = mbar_wait(smem_u32(&ctrl->d_full[pj % ND]), static_cast<uint32_t>(pj / ND) & 1u,
+                         ctx, 8);
+        }
         uint32_t s2 = 0;
         if constexpr (C::kW4) {
           const int slot = ch.ci % SR;
@@ -641,10 +714,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!C::kW4 || seg_last) {
         // drain one accumulator buffer: per group (W8A8) or per segment (W4A16)
-        const int nbuf = C::kW4 ? C::kSegBufs : NB;
         const int idx = C::kW4 ? seg : j;
-        const int b = idx % nbuf;
-        const uint32_t bph = static_cast<uint32_t>(idx / nbuf) & 1u;
+        const int b = idx % ND;
+        const uint32_t bph = static_cast<uint32_t>(idx / ND) & 1u;
         float sw = 0.0f;
         if constexpr (kMode == kModeW8A8) {
           ch.begin(seg_first);
@@ -733,8 +805,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the split tiles this block took part in: the last block to arrive sums
     // the partials and writes the output
     if (named_bar_and(2, C::kEpiThreads, alive)) {
+      uint32_t fix_phase = 0;
       for (int k = 0; k < npend; ++k) {
-        if (split_finish<C::kEpiCols>(p, ctrl, pend[k], nC, colbase, r, et, C::kEpiThreads, acc)) {
+        if (split_finish<C::kEpiCols>(p, ctrl, pend[k], nC, colbase, r, et, C::kEpiThreads, acc,
+                                      sbase, reinterpret_cast<const float*>(smem), sc_off,
+                                      fix_phase, drain_ctx)) {
           const int64_t tt = pend[k].tile / F;
           write_out(tt, (pend[k].tile - tt * F) * kTileF + r, acc);
         }
@@ -859,7 +934,7 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
     ts = tw;  // not read
   }
 
-  const uint32_t fixed = 1024 + C::kScaleBytes + kCtrlBytes;
+  const uint32_t fixed = 1024 + C::kXSlots * C::kABytes + C::kScaleBytes + kCtrlBytes;
   int stages = static_cast<int>((kSmemLimit - fixed) / C::kStageBytes);
   if (stages > kMaxStages) stages = kMaxStages;
   const uint32_t smem = fixed + static_cast<uint32_t>(stages) * C::kStageBytes;
