@@ -236,8 +236,10 @@ class LayerRunner:
         self.gemm_bytes = sum(gemm_algo_bytes(M, K, N, wk) for _, K, N, _, M, wk in specs)
         self.n_actq = len(self.acts)
         self.n_gemm = len(specs)
-        # a W8A8 GEMM call is two launches (int8 -> fp16 operand pass + GEMM)
-        self.n_launches = self.n_actq + sum(2 if wk == "w8a8" else 1 for *_, wk in specs)
+        # one kernel per act-quant and per GEMM, plus the int8 -> fp16 operand
+        # pass of W8A8 GEMMs with token tiles of 96 and more (M > 64)
+        self.n_launches = self.n_actq + sum(2 if (wk == "w8a8" and M > 64) else 1
+                                            for _, _, _, _, M, wk in specs)
 
     def _ikey(self, spec):
         from w4a16_linear_layers_gb300 import synth

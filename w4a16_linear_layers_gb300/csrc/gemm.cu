@@ -17,11 +17,14 @@
 //   * the output is cut into tiles of 128 features x T tokens; the MMA runs
 //     with the weights as operand A (128 rows = features, converted by
 //     threads straight into TMEM) and the tokens as operand B (T columns,
-//     16-bit, loaded by TMA with 128-byte swizzle), so decode-sized M only
+//     16-bit, 128-byte swizzled in shared memory), so decode-sized M only
 //     pads T up to a multiple of 16;
-//   * W8A8 activations are turned from int8 into fp16 once per call by a
-//     small pre-pass kernel (exact), so the GEMM's B operand path is the same
-//     for both formats and no block converts activations;
+//   * W4A16 tokens (bf16) land by TMA directly in the operand layout; W8A8
+//     tokens of tiles up to 64 land as int8 tiles and the converter group of
+//     the step expands them exactly to fp16 beside the weights it converts
+//     (half the bytes from L2, and no extra kernel between act-quant and the
+//     GEMM); larger W8A8 tiles read an exact fp16 image written by a small
+//     pre-pass kernel;
 //   * the work is the list of (tile, group) steps; block c takes the
 //     contiguous range [c*W/C, (c+1)*W/C) of the W steps (stream-K), so every
 //     SM gets the same amount of weight stream whatever the shape;
@@ -31,7 +34,8 @@
 //   * roles: warp 0 streams weights by TMA, warp 2 streams activations and
 //     group scales, warps 1 and 3 issue the MMAs of alternate steps (one
 //     thread's issue rate is below what the weight stream needs), warps 4-11
-//     convert weights into TMEM, warps 12-19 drain TMEM.
+//     convert weights into TMEM (and W8A8 tokens into fp16), warps 12-19
+//     drain TMEM.
 //
 // W8A8 per group g:  D = A_g * B_g (exact integers), then acc = fma(D, s_w, acc)
 // in the epilogue, ascending g; at the end y = bf16(acc * s_a).
@@ -95,12 +99,24 @@ struct Cfg {
   static constexpr int kWordRows = kW4 ? 16 : 32;           // int32 rows per group
   static constexpr uint32_t kWBytes = kWordRows * kTileF * 4;
   static constexpr uint32_t kABytes = 2u * T * 128u;         // two 64-wide 16-bit halves
-  // Weights and activations travel in rings of their own: a weight slot is
-  // freed as soon as the converters have moved it into TMEM, an activation
-  // slot when the MMAs that read it have completed, so neither stream waits
-  // for the other's consumer.  The activation ring is deep enough to cover
-  // the L2 latency seen while the weight stream keeps HBM busy.
+  // Weights and activations travel in rings of their own, so neither stream
+  // waits for the other's consumer.  A weight slot is freed as soon as the
+  // converters have moved it into TMEM.
+  //   W4A16: bf16 activation tiles land by TMA in the MMA's operand layout; a
+  //   slot is freed when the MMAs that read it have completed.
+  //   W8A8, T <= 64: int8 activation tiles land by TMA in a staging ring
+  //   (freed by the converters) and the converter group of the step expands
+  //   them exactly to fp16 in the operand slot that pairs with its A buffer.
+  //   W8A8, T >= 96: that expansion would add ~36 KB of shared-memory traffic
+  //   per step on top of the MMA's own operand reads; a pre-pass kernel
+  //   writes the exact fp16 image once and its tiles land like W4A16's.
+  // The first ring in each case is deep enough to cover the L2 latency seen
+  // while the weight stream keeps HBM busy.
   static constexpr uint32_t kStageBytes = kWBytes;
+  static constexpr uint32_t kXiBytes = static_cast<uint32_t>(T) * 128u;   // int8 tile
+  static constexpr int kXiRaw = static_cast<int>(32768u / kXiBytes);
+  static constexpr bool kXConv = !kW4 && T <= 64;
+  static constexpr int kXiSlots = !kXConv ? 0 : (kXiRaw < 4 ? 4 : (kXiRaw > kMaxXSlots ? kMaxXSlots : kXiRaw));
   static constexpr int kXSlotsRaw = static_cast<int>(65536u / kABytes);
   static constexpr int kXSlotsW4 = kXSlotsRaw < 4 ? 4 : (kXSlotsRaw > kMaxXSlots ? kMaxXSlots : kXSlotsRaw);
   static constexpr int kIssuers = 2;
@@ -120,14 +136,11 @@ struct Cfg {
   // ND - NA even: see the waits of the converters
   static constexpr int kNumD = kW4 ? 1 : kNumDRaw - ((kNumDRaw - kNumBuf) & 1);
   // W8A8 commits once per step, on the step's D buffer: that completion also
-  // frees the step's A buffer and activation slot.  The activation ring then
-  // has one slot per D buffer, so a slot's producer waits for the completion
-  // of the step that last used it, which is always the D buffer's latest
-  // phase (the buffer's next phase needs the very slot being refilled).
-  static constexpr int kXSlots = kW4 ? kXSlotsW4 : kNumD;
+  // frees the step's A buffer and fp16 operand slot (slot i pairs with A
+  // buffer i), which the converters wait for before they refill both.
+  static constexpr int kXSlots = kXConv ? kNumBuf : kXSlotsW4;
   static_assert(kW4 || (kNumD >= kNumBuf && (kNumD - kNumBuf) % 2 == 0),
                 "one commit per step needs ND >= NA with ND - NA even");
-  static_assert(kW4 || kXSlots == kNumD, "activation slot i pairs with D buffer i");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColA = 0;
   static constexpr uint32_t kColD = 64 * kNumBuf;
@@ -167,8 +180,10 @@ struct KParams {
 struct Ctrl {
   uint64_t wfull[kMaxStages];   // the slot's weights landed
   uint64_t empty[kMaxStages];   // the slot's weights are in TMEM
-  uint64_t xfull[kMaxXSlots];   // the slot's activations landed
-  uint64_t xempty[kMaxXSlots];  // the MMAs reading the slot completed
+  uint64_t xfull[kMaxXSlots];   // W4A16: the slot's activations landed;
+                                // W8A8: the staging slot's int8 tile landed
+  uint64_t xempty[kMaxXSlots];  // W4A16: the MMAs reading the slot completed;
+                                // W8A8: the converters read the staging slot
   uint64_t a_full[kBufMax];
   uint64_t a_empty[kBufMax];
   uint64_t d_full[kDBufMax];
@@ -359,9 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const int stages = p.stages;
-  constexpr int NX = C::kXSlots;
+  constexpr int NX = C::kXSlots;                 // 16-bit operand slots
+  constexpr int NXR = C::kXConv ? C::kXiSlots : C::kXSlots;   // slots the producer fills
   const uint32_t x_off = static_cast<uint32_t>(stages) * C::kStageBytes;
-  const uint32_t sc_off = x_off + static_cast<uint32_t>(NX) * C::kABytes;
+  const uint32_t xi_off = x_off + static_cast<uint32_t>(NX) * C::kABytes;
+  const uint32_t sc_off = xi_off + static_cast<uint32_t>(C::kXiSlots) * C::kXiBytes;
   const uint16_t* scale_ring = reinterpret_cast<const uint16_t*>(smem + sc_off);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + sc_off + C::kScaleBytes);
 
@@ -383,9 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->wfull[i]), 1);
       mbar_init(smem_u32(&ctrl->empty[i]), C::kEmptyCount);
     }
-    for (int i = 0; i < NX; ++i) {
+    for (int i = 0; i < NXR; ++i) {
       mbar_init(smem_u32(&ctrl->xfull[i]), 1);
-      mbar_init(smem_u32(&ctrl->xempty[i]), 1);
+      mbar_init(smem_u32(&ctrl->xempty[i]), C::kXConv ? C::kConvWarps / 2 : 1);
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(smem_u32(&ctrl->a_full[i]), C::kConvWarps / 2);
@@ -468,11 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_a);
       if constexpr (C::kScales) prefetch_tmap(&tm_s);
       StepIter it(s0, G, F);
-      Ring rg(NX);
+      Ring rg(NXR);
       ChunkIter ch;
       int issued = 0, s_issued = 0;
       bool waited = false;
-      const int x_first = n_steps < NX ? n_steps : NX;   // loads before the weights resume
+      const int x_first = n_steps < NXR ? n_steps : NXR;   // loads before the weights resume
       bool go = false;
       for (int j = 0; j < n_steps; ++j, it.next(), rg.next(), ch.advance()) {
         if constexpr (C::kScales) {
@@ -488,23 +505,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++s_issued;
           }
         }
-        if constexpr (C::kW4) {
-          if (!mbar_wait(smem_u32(&ctrl->xempty[rg.slot]), rg.phase ^ 1u, ctx, 15)) break;
-        } else if (j >= NX) {
-          // the slot's previous step (j - NX) used D buffer j % ND (NX == ND)
-          if (!mbar_wait(smem_u32(&ctrl->d_full[rg.slot]), rg.phase ^ 1u, ctx, 15)) break;
-        }
+        if (!mbar_wait(smem_u32(&ctrl->xempty[rg.slot]), rg.phase ^ 1u, ctx, 15)) break;
         if (!waited) {
           grid_dep_wait();   // the activations come from the previous kernel
           waited = true;
         }
         const uint32_t full = smem_u32(&ctrl->xfull[rg.slot]);
-        const uint32_t dst = sbase + x_off + static_cast<uint32_t>(rg.slot) * C::kABytes;
-        mbar_arrive_expect_tx(full, C::kABytes);
-        // one load brings both 64-wide halves of the group, each as a T x 128 B
-        // swizzled tile (the activations seen as [K/64 halves][M rows][64])
-        tma_load_3d(dst, &tm_a, full, 0, static_cast<int32_t>(it.t * T),
-                    static_cast<int32_t>(it.g * 2), pol_a);
+        if constexpr (!C::kXConv) {
+          const uint32_t dst = sbase + x_off + static_cast<uint32_t>(rg.slot) * C::kABytes;
+          mbar_arrive_expect_tx(full, C::kABytes);
+          // one load brings both 64-wide halves of the group, each as a T x
+          // 128 B swizzled tile (the activations seen as [K/64][M][64])
+          tma_load_3d(dst, &tm_a, full, 0, static_cast<int32_t>(it.t * T),
+                      static_cast<int32_t>(it.g * 2), pol_a);
+        } else {
+          // the group's int8 tile, T rows x 128 B, 128-byte swizzled
+          const uint32_t dst = sbase + xi_off + static_cast<uint32_t>(rg.slot) * C::kXiBytes;
+          mbar_arrive_expect_tx(full, C::kXiBytes);
+          tma_load_2d(dst, &tm_a, full, static_cast<int32_t>(it.g * kGroup),
+                      static_cast<int32_t>(it.t * T), pol_a);
+        }
         ++issued;
         if (issued == x_first) {
           mbar_arrive(smem_u32(&ctrl->x_go));
@@ -512,8 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!go) mbar_arrive(smem_u32(&ctrl->x_go));
-      for (int j = issued > NX ? issued - NX : 0; j < issued; ++j)
-        (void)mbar_wait(smem_u32(&ctrl->xfull[j % NX]), static_cast<uint32_t>(j / NX) & 1u,
+      for (int j = issued > NXR ? issued - NXR : 0; j < issued; ++j)
+        (void)mbar_wait(smem_u32(&ctrl->xfull[j % NXR]), static_cast<uint32_t>(j / NXR) & 1u,
                         drain_ctx, 16);
       for (int c = s_issued > SR ? s_issued - SR : 0; c < s_issued; ++c)
         (void)mbar_wait(smem_u32(&ctrl->s_full[c % SR]), static_cast<uint32_t>(c / SR) & 1u,
@@ -543,7 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : tmem + C::kColD + db * T;
         if ((j & 1) == me) {
           const bool need_d = C::kW4 ? !started : true;
-          if (!mbar_wait(smem_u32(&ctrl->xfull[rx.slot]), rx.phase, ctx, 3)) break;
+          // in-kernel expansion: a_full also covers the fp16 operand slot
+          // (slot ab, written by the same converter group); else the TMA tile
+          if (!C::kXConv && !mbar_wait(smem_u32(&ctrl->xfull[rx.slot]), rx.phase, ctx, 3)) break;
           if (!mbar_wait(smem_u32(&ctrl->a_full[ab]), abph, ctx, 4)) break;
           if (need_d && !mbar_wait(smem_u32(&ctrl->d_empty[db]), dbph ^ 1u, ctx, 5)) break;
           tc_fence_after();
@@ -560,12 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(dcol, tmem + C::kColA + ab * 64 + ks * 8, d0 + (off >> 4), idesc,
                    acc ? 1u : 0u);
           }
-          if constexpr (C::kW4) {
-            tc_commit(smem_u32(&ctrl->a_empty[ab]));
-            tc_commit(smem_u32(&ctrl->xempty[rx.slot]));
-          } else {
-            tc_commit(smem_u32(&ctrl->d_full[db]));   // also frees A buffer and X slot
-          }
+          if constexpr (C::kW4) tc_commit(smem_u32(&ctrl->a_empty[ab]));
+          if constexpr (!C::kXConv) tc_commit(smem_u32(&ctrl->xempty[rx.slot]));
+          // W8A8: also frees the A buffer (and the fp16 slot of in-kernel expansion)
+          if constexpr (!C::kW4) tc_commit(smem_u32(&ctrl->d_full[db]));
           started = true;
         }
         if constexpr (C::kW4) {
@@ -598,9 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     StepIter it(s0, G, F);
     Ring rg(stages);
+    Ring ri(C::kXConv ? NXR : 1);   // in-kernel expansion: int8 staging slot of the step
     ChunkIter ch;
     bool chunk_ready = false;   // W4A16: this group has waited for the chunk's scales
-    for (int j = 0; j < n_steps; ++j, it.next(), rg.next(), ch.advance()) {
+    for (int j = 0; j < n_steps; ++j, it.next(), rg.next(), ri.next(), ch.advance()) {
       const bool seg_last = (j == n_steps - 1) || (it.g == G - 1);
       if constexpr (C::kW4) {
         if (ch.begin(j == 0 || it.g == 0)) chunk_ready = false;
@@ -621,6 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(smem_u32(&ctrl->d_full[pj % ND]), static_cast<uint32_t>(pj / ND) & 1u,
                          ctx, 8);
         }
+        if (C::kXConv && ok) ok = mbar_wait(smem_u32(&ctrl->xfull[ri.slot]), ri.phase, ctx, 3);
         uint32_t s2 = 0;
         if constexpr (C::kW4) {
           const int slot = ch.ci % SR;
@@ -635,6 +657,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!warp_all(ok)) break;
         }
         tc_fence_after();
+        if constexpr (C::kXConv) {
+          // The step's int8 tokens (T rows x 128, 128-byte swizzled) become
+          // the fp16 B operand in slot ab: two 64-wide halves of T rows x
+          // 128 B, 128-byte swizzled.  q + 128 as a biased byte -> exact fp16.
+          const uint8_t* xi = smem + xi_off + static_cast<uint32_t>(ri.slot) * C::kXiBytes;
+          uint8_t* xf = smem + x_off + static_cast<uint32_t>(ab) * C::kABytes;
+#pragma unroll
+          for (int q = r; q < 8 * T; q += kTileF) {
+            const int row = q >> 3;      // token row of the tile
+            const int c = q & 7;         // 16-byte chunk = 16 K values
+            const uint4 raw = *reinterpret_cast<const uint4*>(xi + row * 128 + ((c ^ (row & 7)) << 4));
+            uint4 o0, o1;
+            biased_u8x4_to_f16x4(raw.x ^ 0x80808080u, o0.x, o0.y);
+            biased_u8x4_to_f16x4(raw.y ^ 0x80808080u, o0.z, o0.w);
+            biased_u8x4_to_f16x4(raw.z ^ 0x80808080u, o1.x, o1.y);
+            biased_u8x4_to_f16x4(raw.w ^ 0x80808080u, o1.z, o1.w);
+            uint8_t* dst = xf + (c >> 2) * (T * 128) + row * 128;
+            const int c2 = (c & 3) * 2;
+            *reinterpret_cast<uint4*>(dst + ((c2 ^ (row & 7)) << 4)) = o0;
+            *reinterpret_cast<uint4*>(dst + (((c2 + 1) ^ (row & 7)) << 4)) = o1;
+          }
+          fence_proxy_async_smem();   // generic writes -> the MMA's async reads
+        }
         const uint32_t* wsm = reinterpret_cast<const uint32_t*>(
             smem + static_cast<uint32_t>(rg.slot) * C::kStageBytes);
         const uint32_t acol = tmem + lane_off + C::kColA + ab * 64;
@@ -657,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(smem_u32(&ctrl->empty[rg.slot]));
+          if constexpr (C::kXConv) mbar_arrive(smem_u32(&ctrl->xempty[ri.slot]));
           mbar_arrive(smem_u32(&ctrl->a_full[ab]));
         }
       }
@@ -827,9 +873,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// int8 activations -> fp16 (exact), 16 values per thread; the W8A8 GEMM's B
-// operand.  Waits for its predecessor before touching memory (the previous
-// GEMM may still read this buffer), then lets the GEMM start.
+// int8 activations -> fp16 (exact), 16 values per thread: the B operand of
+// the W8A8 GEMM at token tiles of 96 and more.  Waits for its predecessor
+// before touching memory (the previous GEMM may still read this buffer), then
+// lets the GEMM start.
 __global__ void __launch_bounds__(256) act_i8_to_f16_kernel(const int8_t* __restrict__ q,
                                                             uint16_t* __restrict__ out,
                                                             int64_t n16) {
@@ -904,7 +951,7 @@ template <int kMode, int T>
 cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream_t stream) {
   using C = Cfg<kMode, T>;
   const void* act16 = a.act;
-  if constexpr (!C::kW4) {
+  if constexpr (!C::kW4 && !C::kXConv) {
     // int8 activations -> fp16 image in the workspace
     uint16_t* dst = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.workspace) + pl.act_offset);
     const int64_t n16 = a.M * a.K / 16;
@@ -921,9 +968,16 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
                    static_cast<uint64_t>(a.N) * 4, kTileF, C::kWordRows,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (!make_act_map(&ta, C::kW4 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                    act16, a.M, a.K, T))
-    return cudaErrorInvalidValue;
+  if constexpr (!C::kXConv) {
+    if (!make_act_map(&ta, C::kW4 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      act16, a.M, a.K, T))
+      return cudaErrorInvalidValue;
+  } else {
+    // int8 q_a [M][K]: one box is a 128-wide group of T rows, 128-byte swizzled
+    if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.act, a.K, a.M, a.K, kGroup, T,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   CUtensorMap ts;
   if constexpr (C::kScales) {
     if (!make_map_2d(&ts, C::kW4 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -934,7 +988,8 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
     ts = tw;  // not read
   }
 
-  const uint32_t fixed = 1024 + C::kXSlots * C::kABytes + C::kScaleBytes + kCtrlBytes;
+  const uint32_t fixed = 1024 + C::kXSlots * C::kABytes + C::kXiSlots * C::kXiBytes +
+                         C::kScaleBytes + kCtrlBytes;
   int stages = static_cast<int>((kSmemLimit - fixed) / C::kStageBytes);
   if (stages > kMaxStages) stages = kMaxStages;
   const uint32_t smem = fixed + static_cast<uint32_t>(stages) * C::kStageBytes;
@@ -999,9 +1054,11 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
   // any shape that share a workspace never see each other's partials there.
   p.counter_bytes = kCounterBytes;
   const size_t partial_bytes = static_cast<size_t>(p.ctas) * 2 * p.T * kTileF * sizeof(float);
-  // then the fp16 image of the W8A8 activations (1 KB aligned)
+  // then, for token tiles of 96 and more, the fp16 image of the W8A8
+  // activations (1 KB aligned)
   p.act_offset = (p.counter_bytes + partial_bytes + 1023) & ~static_cast<size_t>(1023);
-  p.workspace_bytes = p.act_offset + static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
+  p.workspace_bytes = p.T >= 96 ? p.act_offset + static_cast<size_t>(M) * static_cast<size_t>(K) * 2
+                                : p.counter_bytes + partial_bytes;
   return p;
 }
 

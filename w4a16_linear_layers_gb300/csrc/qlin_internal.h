@@ -51,7 +51,7 @@ struct GemmPlan {
   int64_t steps;   // TT * F * G
   int64_t ctas;    // grid size
   size_t counter_bytes;
-  size_t act_offset;     // fp16 image of the W8A8 activations in the workspace
+  size_t act_offset;     // fp16 image of the W8A8 activations (token tiles >= 96)
   size_t workspace_bytes;
 };
 
