@@ -294,7 +294,20 @@ def time_graph(torch, graph, reps):
     return start.elapsed_time(end) / 1e3  # seconds
 
 
+# Workloads whose CUDA-graph replay is disabled: the prefill graph (W8A8 GEMMs
+# with 128-token tiles, M up to 8192) faulted the GPU after tens of
+# back-to-back replays while every single replay, and every shape run alone,
+# passed.  Until the cause is found it is not replayed; its shapes stay
+# covered by the parity tests (eager calls).
+DISABLED_WORKLOADS = {
+    "prefill": "graph replay of the prefill step faulted the GPU (unspecified launch "
+               "failure after tens of back-to-back replays); disabled until the cause is found",
+}
+
+
 def run_ours(args, rank, world, local_rank):
+    if args.workload in DISABLED_WORKLOADS:
+        raise SystemExit(f"workload {args.workload!r} is disabled: {DISABLED_WORKLOADS[args.workload]}")
     import torch
     from w4a16_linear_layers_gb300 import build as qbuild
     from w4a16_linear_layers_gb300 import qlin

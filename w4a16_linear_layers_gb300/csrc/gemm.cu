@@ -333,8 +333,11 @@ __device__ __forceinline__ bool split_finish(const KParams& p, Ctrl* ctrl, const
     const int64_t nb = (c_last - b0 + 1) < cap ? (c_last - b0 + 1) : cap;
     if (et == 0) {
       // the rings were last touched by generic loads and stores (converters,
-      // the previous batch's sums): order those before the async copies
+      // the previous batch's sums), and the partials were written by other
+      // blocks' generic stores (acquired through the arrival counter): order
+      // both before the async copies
       fence_proxy_async_smem();
+      fence_proxy_async_global();
       const uint32_t full = smem_u32(&ctrl->fix_full);
       mbar_arrive_expect_tx(full, static_cast<uint32_t>(nb) * kPartBytes);
       for (int64_t i = 0; i < nb; ++i) {
