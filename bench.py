@@ -163,12 +163,14 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, fused):
     """DRAM bytes per GEMM launch from the committed ncu summary of this
-    workload, or None when the GEMM sources changed since that capture (the
-    summary records the sha256 prefix of the sources it measured)."""
+    workload and call list (fused or one GEMM per linear), or None when the
+    GEMM sources changed since that capture (the summary records the sha256
+    prefix of the sources it measured)."""
     if workload != "layer":
         return None
+    key = "traffic_bytes_per_launch_fused:" if fused else "traffic_bytes_per_launch:"
     import hashlib
     csrc = os.path.join(ROOT, "w4a16_linear_layers_gb300", "csrc")
     h = hashlib.sha256()
@@ -183,7 +185,7 @@ def profiled_traffic(workload):
     if h.hexdigest()[:16] not in text:
         return None
     for line in text.splitlines():
-        if line.startswith("traffic_bytes_per_launch:"):
+        if line.startswith(key):
             return int(line.split(":")[1])
     return None
 
@@ -191,7 +193,12 @@ def profiled_traffic(workload):
 # ---------------------------------------------------------------- our arm
 
 class LayerRunner:
-    """Device-resident weights and inputs for a workload, and one step."""
+    """Device-resident weights and inputs for a workload, and one step.
+
+    With fuse, projections that read the same input (q/k/v, gate/up) run as
+    one GEMM over their weights concatenated along N: the same bytes and
+    outputs (output columns are independent), fewer launches.  The unfused
+    call list is kept beside it so both can be timed."""
 
     def __init__(self, specs, device, seed=0):
         import torch
@@ -205,7 +212,6 @@ class LayerRunner:
         self.weights = {}
         self.inputs = {}
         self.acts = {}
-        self.outputs = []
         for name, K, N, kind, M, wk in specs:
             key = (name, wk)
             if key not in self.weights:
@@ -221,25 +227,55 @@ class LayerRunner:
                     sd = torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).to(device)
                 del qd
                 self.weights[key] = (qw, sd)
-            ikey = (synth.shared_input_name(name), M, K, kind)
+            ikey = self._ikey((name, K, N, kind, M, wk))
             if ikey not in self.inputs:
                 xb = synth.activations(seed, f"{ikey[0]}/M{M}", M, K, kind)
                 self.inputs[ikey] = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(device)
                 if wk == "w8a8":
                     self.acts[ikey] = (torch.empty((M, K), dtype=torch.int8, device=device),
                                        torch.empty((M,), dtype=torch.float32, device=device))
-            self.outputs.append(torch.empty((M, N), dtype=torch.bfloat16, device=device))
-            self.ws.get(M, N, K)
+        # unfused: one call per linear; fused: one call per (input, format)
+        self.calls = {False: [], True: []}
+        groups = {}
+        for spec in specs:
+            name, K, N, kind, M, wk = spec
+            self.calls[False].append(self._call(wk, self._ikey(spec), [name], M, K))
+            groups.setdefault((self._ikey(spec), wk), []).append(name)
+        for (ikey, wk), names in groups.items():
+            self.calls[True].append(self._call(wk, ikey, names, ikey[1], ikey[2]))
         torch.cuda.synchronize()
         self.weight_bytes = sum(weight_bytes(K, N, wk) for _, K, N, _, _, wk in specs)
         self.ops = sum(2 * M * K * N for _, K, N, _, M, _ in specs)
-        self.gemm_bytes = sum(gemm_algo_bytes(M, K, N, wk) for _, K, N, _, M, wk in specs)
         self.n_actq = len(self.acts)
-        self.n_gemm = len(specs)
+
+    def _call(self, wk, ikey, names, M, K):
+        torch = self.torch
+        parts = [self.weights[(n, wk)] for n in names]
+        if len(parts) == 1:
+            qw, sc = parts[0]
+        else:
+            qw = torch.cat([p[0] for p in parts], dim=1).contiguous()
+            sc = torch.cat([p[1] for p in parts], dim=1).contiguous()
+        N = qw.shape[1]
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=self.device)
+        self.ws.get(M, N, K)
+        return {"wk": wk, "ikey": ikey, "qw": qw, "sc": sc, "y": y, "M": M, "N": N, "K": K,
+                "names": names}
+
+    def outputs(self, fused):
+        return [c["y"] for c in self.calls[fused]]
+
+    def n_gemm(self, fused):
+        return len(self.calls[fused])
+
+    def gemm_bytes(self, fused):
+        return sum(gemm_algo_bytes(c["M"], c["K"], c["N"], c["wk"]) for c in self.calls[fused])
+
+    def n_launches(self, fused):
         # one kernel per act-quant and per GEMM, plus the int8 -> fp16 operand
         # pass of W8A8 GEMMs with token tiles of 96 and more (M > 64)
-        self.n_launches = self.n_actq + sum(2 if (wk == "w8a8" and M > 64) else 1
-                                            for _, _, _, _, M, wk in specs)
+        return self.n_actq + sum(2 if (c["wk"] == "w8a8" and c["M"] > 64) else 1
+                                 for c in self.calls[fused])
 
     def _ikey(self, spec):
         from w4a16_linear_layers_gb300 import synth
@@ -251,21 +287,19 @@ class LayerRunner:
         for ikey, (q, s) in self.acts.items():
             self.qlin.act_quant_i8(self.inputs[ikey], q, s)
 
-    def gemms(self):
+    def gemms(self, fused=False):
         ws = self.ws.buf
-        for spec, y in zip(self.specs, self.outputs):
-            name, K, N, kind, M, wk = spec
-            qw, sc = self.weights[(name, wk)]
-            ikey = self._ikey(spec)
-            if wk == "w8a8":
-                q, s = self.acts[ikey]
-                self.qlin.gemm_w8a8_gs128(q, s, qw, sc, y, workspace=ws)
+        for c in self.calls[fused]:
+            if c["wk"] == "w8a8":
+                q, s = self.acts[c["ikey"]]
+                self.qlin.gemm_w8a8_gs128(q, s, c["qw"], c["sc"], c["y"], workspace=ws)
             else:
-                self.qlin.gemm_w4a16_g128(self.inputs[ikey], qw, sc, y, workspace=ws)
+                self.qlin.gemm_w4a16_g128(self.inputs[c["ikey"]], c["qw"], c["sc"], c["y"],
+                                          workspace=ws)
 
-    def step(self):
+    def step(self, fused=False):
         self.quantize()
-        self.gemms()
+        self.gemms(fused)
 
     def capture(self, fn):
         torch = self.torch
@@ -321,8 +355,11 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
 
-    step_graph = runner.capture(runner.step)
-    gemm_graph = runner.capture(runner.gemms)
+    fused = not args.no_fuse
+    step_graph = runner.capture(lambda: runner.step(fused))
+    gemm_graph = runner.capture(lambda: runner.gemms(fused))
+    # the other call list (unfused when the headline is fused), timed beside it
+    alt_graph = runner.capture(lambda: runner.step(not fused)) if runner.n_gemm(True) != runner.n_gemm(False) else None
     # Bring the clocks up from idle before the warm-up proper (untimed).
     t_soak = time.perf_counter()
     while time.perf_counter() - t_soak < args.soak:
@@ -343,24 +380,26 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     t_step = time_graph(torch, step_graph, args.steps)
     t_gemm = time_graph(torch, gemm_graph, args.steps)
+    t_alt = time_graph(torch, alt_graph, args.steps) if alt_graph is not None else 0.0
     clock_info = clocks.stop()
     if dist:
-        t = torch.tensor([t_step, t_gemm], device=device, dtype=torch.float64)
+        t = torch.tensor([t_step, t_gemm, t_alt], device=device, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, t_gemm = t.tolist()
+        t_step, t_gemm, t_alt = t.tolist()
 
     # end to end through the binding: inputs copied from pinned host memory,
     # outputs copied back, every step, no graph
     host_in = {k: v.cpu().pin_memory() for k, v in runner.inputs.items()}
-    host_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in runner.outputs]
+    outs = runner.outputs(fused)
+    host_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in outs]
     h2d = sum(v.numel() * 2 for v in host_in.values())
-    d2h = sum(y.numel() * 2 for y in runner.outputs)
+    d2h = sum(y.numel() * 2 for y in outs)
 
     def e2e_step():
         for k, v in host_in.items():
             runner.inputs[k].copy_(v, non_blocking=True)
-        runner.step()
-        for h, y in zip(host_out, runner.outputs):
+        runner.step(fused)
+        for h, y in zip(host_out, outs):
             h.copy_(y, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -385,8 +424,8 @@ def run_ours(args, rank, world, local_rank):
     ms = t_step / args.steps * 1e3
     value = runner.weight_bytes * args.steps * world / t_step / 1e9
     hbm, bf16, peak_src = measured_peaks()
-    gemm_avg_s = t_gemm / (args.steps * runner.n_gemm)
-    bytes_per_launch = runner.gemm_bytes / runner.n_gemm
+    gemm_avg_s = t_gemm / (args.steps * runner.n_gemm(fused))
+    bytes_per_launch = runner.gemm_bytes(fused) / runner.n_gemm(fused)
     achieved = bytes_per_launch / gemm_avg_s / 1e9
     line = {
         "metric": "W8A8-GS128 linear weight GB/s (TOPS beside it); % of HBM roofline",
@@ -403,7 +442,11 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded splitmix64; weights uniform int8, fp16 log-uniform scales)",
         "config": {
             "workload": WORKLOAD_DESC[args.workload],
-            "linears_per_step": runner.n_gemm,
+            "linears_per_step": len(runner.specs),
+            "gemm_launches_per_step": runner.n_gemm(fused),
+            "fused_projections": ("projections that read the same input (q/k/v, gate/up) run as one "
+                                  "GEMM over their weights concatenated along N: same bytes and outputs"
+                                  if fused else "off: one GEMM per linear"),
             "act_quant_per_step": runner.n_actq,
             "weight_bytes_per_step": runner.weight_bytes,
             "tops": round(runner.ops * args.steps * world / t_step / 1e12, 3),
@@ -413,7 +456,7 @@ def run_ours(args, rank, world, local_rank):
                       "untimed soak before the warm-up steps",
             "parallelism": f"replicas x{world}",
         },
-        "gpu_launches": runner.n_launches * args.steps,
+        "gpu_launches": runner.n_launches(fused) * args.steps,
         "roofline": {
             "bound": "hbm",
             "kernel": "qlin_gemm_kernel (W8A8 GS128)",
@@ -422,7 +465,7 @@ def run_ours(args, rank, world, local_rank):
             "peak_source": peak_src,
             "unit": "GB/s",
             "frac": round(achieved / hbm, 4),
-            "traffic": profiled_traffic(args.workload),
+            "traffic": profiled_traffic(args.workload, fused),
             "bytes_per_launch": round(bytes_per_launch),
             "avg_launch_us": round(gemm_avg_s * 1e6, 3),
         },
@@ -434,6 +477,12 @@ def run_ours(args, rank, world, local_rank):
             "ms_per_step": round(t_e2e * 1e3, 4),
         },
         "clocks": clock_info,
+        "other_call_list": (None if alt_graph is None else {
+            "fused_projections": not fused,
+            "value": round(runner.weight_bytes * args.steps * world / t_alt / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(t_alt / args.steps * 1e3, 4),
+            "gemm_launches_per_step": runner.n_gemm(not fused)}),
     }
     return line, runner
 
@@ -554,6 +603,8 @@ def main():
                     help="seconds of untimed replays before the warm-up (clock ramp)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="layer", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--no-fuse", action="store_true",
+                    help="one GEMM per linear (default: projections sharing an input run as one GEMM)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     args = ap.parse_args()

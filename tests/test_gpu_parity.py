@@ -216,6 +216,37 @@ def test_w4a16_matches_oracle(M, K, N):
     compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), f"w4a16 {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("fmt,M", [("w8a8", 8), ("w8a8", 64), ("w8a8", 96), ("w4a16", 8), ("w4a16", 64)])
+def test_fused_projections_match_each_oracle(fmt, M):
+    """Projections that read one input (q/k/v, gate/up) run as one GEMM over
+    their packed weights and scales concatenated along N; each column block
+    of the output must match the oracle of its own projection."""
+    K, Ns = 640, (256, 128, 136)
+    xb = synth.activations(12, f"gpu/fused/{fmt}/{M}/x", M, K, "outliers" if fmt == "w8a8" else "normal")
+    parts = []
+    for i, N in enumerate(Ns):
+        if fmt == "w8a8":
+            qwt, sc = synth.w8a8_weights(12, f"gpu/fused/{fmt}/w{i}", K, N)
+            qw, _, _ = oracle.pack_gptq(qwt, 8)
+        else:
+            qwt, sc = synth.w4a16_weights(12, f"gpu/fused/{fmt}/w{i}", K, N)
+            qw, _, _ = oracle.pack_gptq(qwt, 4)
+        parts.append((qw, sc))
+    qw_cat = np.concatenate([p[0] for p in parts], axis=1)
+    sc_cat = np.concatenate([p[1] for p in parts], axis=1)
+    if fmt == "w8a8":
+        qa, sa = oracle.act_quant_i8(xb)
+        y = _gemm_w8a8_gpu(qa, sa, qw_cat, sc_cat)
+    else:
+        y = _gemm_w4a16_gpu(xb, qw_cat, sc_cat)
+    off = 0
+    for i, ((qw, sc), N) in enumerate(zip(parts, Ns)):
+        ref = (oracle.gemm_w8a8_gs128(qa, sa, qw, sc, K) if fmt == "w8a8"
+               else oracle.gemm_w4a16_g128(xb, qw, sc, K))
+        compare_linear(np.ascontiguousarray(y[:, off:off + N]), ref, f"fused {fmt} M={M} part {i}")
+        off += N
+
+
 def test_w4a16_identity_probe_bit_exact():
     K, N = 256, 384
     _, qwt, qw, sb = _w4a16_inputs(10, "gpu/w4/probe", 1, K, N)
