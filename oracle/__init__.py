@@ -16,6 +16,7 @@ patterns):
 * ``gemm_w8a8_gs128(...)``            -> dict of y_bf16 / y_f32 / y64 / bound
 * ``gemm_w4a16_g128(...)``            -> same dict
 * ``dequant_w4a16(qweight, scales, K, N)`` -> w bf16 bits [K,N]
+* ``argmax_bf16_rows(y_bits)``        -> int32 [M], greedy token per row
 """
 from __future__ import annotations
 
@@ -78,6 +79,8 @@ def _load():
             lib.orc_gemm_w4a16_g128.restype = None
             lib.orc_dequant_w4a16.argtypes = [P, P, I, I, P]
             lib.orc_dequant_w4a16.restype = None
+            lib.orc_argmax_bf16_rows.argtypes = [P, I, I, P]
+            lib.orc_argmax_bf16_rows.restype = None
             _lib = lib
     return _lib
 
@@ -209,3 +212,13 @@ def dequant_w4a16(qweight, scales_bf16_bits, K: int, N: int) -> np.ndarray:
     w = np.empty((K, N), np.uint16)
     _load().orc_dequant_w4a16(_ptr(qw), _ptr(sc), K, N, _ptr(w))
     return w
+
+
+def argmax_bf16_rows(y_bits) -> np.ndarray:
+    """Greedy token per row of a bf16 output: index of the largest value,
+    the lowest index on ties."""
+    y = _c(y_bits, np.uint16)
+    M, N = y.shape
+    idx = np.empty(M, np.int32)
+    _load().orc_argmax_bf16_rows(_ptr(y), M, N, _ptr(idx))
+    return idx

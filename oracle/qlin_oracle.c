@@ -283,3 +283,24 @@ void orc_dequant_w4a16(const int32_t *qweight, const uint16_t *scales_bf16,
             w_bf16[k * N + n] = orc_f32_to_bf16((float)weight_at(qweight, N, 4, k, n) * s);
         }
 }
+
+/* Greedy decoding reads only the argmax of the vocabulary head's output
+ * ("DFlash2 decoding" recipe page: single-GPU, batch-one greedy inference,
+ * with an INT8 or INT4 group-128 shared vocabulary head): for each row m of
+ * y (bf16 [M, N]) the index n of the largest value, the lowest such index
+ * when several are equal.  Values compare as the numbers they encode. */
+void orc_argmax_bf16_rows(const uint16_t *y, int64_t M, int64_t N, int32_t *idx)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        int64_t best = 0;
+        float best_v = orc_bf16_to_f32(y[m * N]);
+        for (int64_t n = 1; n < N; ++n) {
+            const float v = orc_bf16_to_f32(y[m * N + n]);
+            if (v > best_v) {
+                best_v = v;
+                best = n;
+            }
+        }
+        idx[m] = (int32_t)best;
+    }
+}

@@ -358,3 +358,27 @@ def test_w4a16_fp64_invariant(oracle_lib):
     assert np.allclose(out["y64"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
     assert np.all(np.abs(out["y_f32"].astype(np.float64) - out["y64"]) <= out["bound"])
     assert np.array_equal(out["y_bf16"], bf16_of(out["y_f32"]))
+
+
+# ------------------------------------------------------------- greedy argmax
+
+def test_argmax_rows_hand_cases(oracle_lib):
+    """Largest value per row, lowest index on ties; -0 and +0 are equal."""
+    y = synth.bf16_bits(np.array([
+        [-1.0, -0.5, -0.5, -2.0],     # tie between 1 and 2 -> 1
+        [2.0, 2.0, 1.0, 2.0],         # three-way tie -> 0
+        [-0.0, 0.0, -0.0, 0.0],       # signed zeros compare equal -> 0
+        [-3.0, -2.0, -7.0, -2.0],     # all negative -> 1
+        [1.0, 1.0078125, 1.0, 0.5],   # one bf16 ulp above 1 -> 1
+    ], np.float32))
+    assert oracle_lib.argmax_bf16_rows(y).tolist() == [1, 0, 0, 1, 1]
+
+
+def test_argmax_rows_matches_numpy_first_max(oracle_lib):
+    """Against numpy's argmax of the decoded values (first maximum), on rows
+    with many exact ties (few distinct values)."""
+    rng = np.random.default_rng(3)
+    vals = rng.integers(-4, 5, size=(64, 1000)).astype(np.float32) * 0.25
+    y = synth.bf16_bits(vals)
+    want = np.argmax(synth.bf16_values(y).astype(np.float64), axis=1)
+    assert np.array_equal(oracle_lib.argmax_bf16_rows(y), want.astype(np.int32))
