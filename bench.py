@@ -65,6 +65,9 @@ def workload_specs(name: str):
     elif name == "vocab":
         for M in (8, 96):
             specs.append(("lm_head", 5120, 248320, "outliers", M, "w8a8"))
+    elif name == "vocab_argmax":
+        for M in (8, 96):
+            specs.append(("lm_head", 5120, 248320, "outliers", M, "w8a8_argmax"))
     else:
         raise SystemExit(f"unknown workload {name}")
     return specs
@@ -77,19 +80,24 @@ WORKLOAD_DESC = {
     "w4a16": "full drafter in W4A16 g128 (36 linears), M in {8,64}",
     "prefill": "W8A8 GS128 gate/up 5120->17408 + down 17408->5120, M in {128,512,2048,8192}",
     "vocab": "W8A8 GS128 vocab head 5120->248320, M in {8,96}",
+    "vocab_argmax": "W8A8 GS128 vocab head 5120->248320 with fused greedy argmax, M in {8,96}",
 }
 
 
 def weight_bytes(K, N, kind):
+    kind = kind.replace("_argmax", "")
     return (K * N if kind == "w8a8" else K * N // 2) + 2 * (K // 128) * N
 
 
 def gemm_algo_bytes(M, K, N, kind):
     """Algorithmic bytes of one GEMM launch: weights + scales once, the
     activation operand once (int8 for W8A8, bf16 for W4A16), activation
-    scales, and the bf16 output."""
+    scales, and the output (bf16 y, or one int32 index per row for the
+    greedy-argmax variant)."""
+    out = 4 * M if kind.endswith("_argmax") else 2 * M * N
+    kind = kind.replace("_argmax", "")
     act = M * K * (1 if kind == "w8a8" else 2) + (4 * M if kind == "w8a8" else 0)
-    return weight_bytes(K, N, kind) + act + 2 * M * N
+    return weight_bytes(K, N, kind) + act + out
 
 
 # -------------------------------------------------------------------- clocks
@@ -215,7 +223,7 @@ class LayerRunner:
         for name, K, N, kind, M, wk in specs:
             key = (name, wk)
             if key not in self.weights:
-                if wk == "w8a8":
+                if wk.startswith("w8a8"):
                     q, s = synth.w8a8_weights(seed, name, K, N)
                     qd = torch.from_numpy(q).to(device)
                     qw, _ = qlin.pack_gptq(qd, 8, with_qzeros=False)
@@ -231,7 +239,7 @@ class LayerRunner:
             if ikey not in self.inputs:
                 xb = synth.activations(seed, f"{ikey[0]}/M{M}", M, K, kind)
                 self.inputs[ikey] = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(device)
-                if wk == "w8a8":
+                if wk.startswith("w8a8"):
                     self.acts[ikey] = (torch.empty((M, K), dtype=torch.int8, device=device),
                                        torch.empty((M,), dtype=torch.float32, device=device))
         # unfused: one call per linear; fused: one call per (input, format)
@@ -257,7 +265,10 @@ class LayerRunner:
             qw = torch.cat([p[0] for p in parts], dim=1).contiguous()
             sc = torch.cat([p[1] for p in parts], dim=1).contiguous()
         N = qw.shape[1]
-        y = torch.empty((M, N), dtype=torch.bfloat16, device=self.device)
+        if wk.endswith("_argmax"):     # greedy token per row
+            y = torch.empty((M,), dtype=torch.int32, device=self.device)
+        else:
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=self.device)
         self.ws.get(M, N, K)
         return {"wk": wk, "ikey": ikey, "qw": qw, "sc": sc, "y": y, "M": M, "N": N, "K": K,
                 "names": names}
@@ -274,8 +285,8 @@ class LayerRunner:
     def n_launches(self, fused):
         # one kernel per act-quant and per GEMM, plus the int8 -> fp16 operand
         # pass of W8A8 GEMMs with token tiles of 96 and more (M > 64)
-        return self.n_actq + sum(2 if (c["wk"] == "w8a8" and c["M"] > 64) else 1
-                                 for c in self.calls[fused])
+        return self.n_actq + sum(1 + (c["wk"].startswith("w8a8") and c["M"] > 64)
+                                 + c["wk"].endswith("_argmax") for c in self.calls[fused])
 
     def _ikey(self, spec):
         from w4a16_linear_layers_gb300 import synth
@@ -290,7 +301,10 @@ class LayerRunner:
     def gemms(self, fused=False):
         ws = self.ws.buf
         for c in self.calls[fused]:
-            if c["wk"] == "w8a8":
+            if c["wk"] == "w8a8_argmax":
+                q, s = self.acts[c["ikey"]]
+                self.qlin.gemm_w8a8_gs128_argmax(q, s, c["qw"], c["sc"], c["y"], workspace=ws)
+            elif c["wk"] == "w8a8":
                 q, s = self.acts[c["ikey"]]
                 self.qlin.gemm_w8a8_gs128(q, s, c["qw"], c["sc"], c["y"], workspace=ws)
             else:
@@ -393,7 +407,7 @@ def run_ours(args, rank, world, local_rank):
     outs = runner.outputs(fused)
     host_out = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in outs]
     h2d = sum(v.numel() * 2 for v in host_in.values())
-    d2h = sum(y.numel() * 2 for y in outs)
+    d2h = sum(y.numel() * y.element_size() for y in outs)
 
     def e2e_step():
         for k, v in host_in.items():
@@ -513,14 +527,14 @@ def oracle_sample(specs, budget_s, seed=0, cache=None):
     def operands(name, K, N, kind, M, wk, nc):
         key = (name, wk)
         if key not in cache:
-            if wk == "w8a8":
+            if wk.startswith("w8a8"):
                 cache[key] = synth.w8a8_weights(seed, name, K, N)
             else:
                 cache[key] = synth.w4a16_weights(seed, name + "/w4", K, N)
         q, s = cache[key]
         q, s = np.ascontiguousarray(q[:, :nc]), np.ascontiguousarray(s[:, :nc])
         xb = synth.activations(seed, f"{synth.shared_input_name(name)}/M{M}", M, K, kind)
-        if wk == "w8a8":
+        if wk.startswith("w8a8"):
             qw, _, _ = oracle.pack_gptq(q, 8)
             qa, sa = oracle.act_quant_i8(xb)
             return (lambda ch, a=(qa, sa, qw, s, K): oracle.gemm_w8a8_gs128(*a, cols=ch))

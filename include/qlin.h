@@ -171,6 +171,37 @@ qlin_status_t qlin_gemm_w4a16_g128(const uint16_t *x, const int32_t *qweight,
                                    size_t workspace_bytes, qlin_stream_t stream);
 
 /*
+ * Vocabulary head with fused greedy argmax: the same linear as
+ * qlin_gemm_w8a8_gs128 / qlin_gemm_w4a16_g128, but instead of y the call
+ * returns, per row m, the column index of the largest bf16 output value (the
+ * lowest index on ties; -0 equals +0).  y itself is never written.
+ *
+ * Passages: "DFlash2 decoding" recipe page (Eole), which runs single-GPU,
+ * batch-one greedy inference with an INT8 or INT4 group-128 shared
+ * vocabulary head; the Flint card's INT8 LM head switch.  Greedy decoding
+ * needs only the argmax.
+ *
+ *   arguments as for the matching GEMM, except:
+ *   argmax   int32 [M]             device; 4-byte aligned
+ *   M        at most 128 (one token tile); larger M returns QLIN_ERR_SHAPE
+ *   workspace / workspace_bytes    at least qlin_workspace_bytes(M, N, K)
+ *
+ * Each output value is the bit-identical bf16 value the matching GEMM call
+ * writes for the same (M, N, K) on the same device, so the index equals the
+ * argmax of that call's y.  Asynchronous on `stream`.  Calls that share a
+ * workspace must not overlap.
+ */
+qlin_status_t qlin_gemm_w8a8_gs128_argmax(const int8_t *q_a, const float *s_a,
+                                          const int32_t *qweight, const uint16_t *scales,
+                                          int64_t M, int64_t N, int64_t K, int32_t *argmax,
+                                          void *workspace, size_t workspace_bytes,
+                                          qlin_stream_t stream);
+qlin_status_t qlin_gemm_w4a16_g128_argmax(const uint16_t *x, const int32_t *qweight,
+                                          const uint16_t *scales, int64_t M, int64_t N,
+                                          int64_t K, int32_t *argmax, void *workspace,
+                                          size_t workspace_bytes, qlin_stream_t stream);
+
+/*
  * GPTQ packer (offline step; not on the timed path).
  *
  * Passages: "Flint-DFlash2-GPTQ-INT8-PTQR" card, parameter table (GPTQ

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import compare_linear, from_dev_bits, to_dev, to_dev_bits
+from helpers import bf16_ulp, compare_linear, from_dev_bits, to_dev, to_dev_bits
 from w4a16_linear_layers_gb300 import qlin, synth
 from w4a16_linear_layers_gb300 import build as qbuild
 
@@ -299,3 +299,60 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     q, s = _act_quant_gpu(xb)
     oq, _ = oracle.act_quant_i8(xb)
     assert np.array_equal(q, oq)
+
+
+# ---------------------------------------------------- fused greedy argmax
+
+def _argmax_case(fmt, M, K, N, seed=13):
+    if fmt == "w8a8":
+        xb, qa, sa, _, qw, sc = _w8a8_inputs(seed, f"gpu/amax/{M}/{K}/{N}", M, K, N)
+        y = _gemm_w8a8_gpu(qa, sa, qw, sc)
+        idx = qlin.gemm_w8a8_gs128_argmax(to_dev(qa), to_dev(sa), to_dev(qw),
+                                          to_dev_bits(sc, torch.float16))
+        ref = oracle.gemm_w8a8_gs128(qa, sa, qw, sc, K)
+    else:
+        xb, _, qw, sc = _w4a16_inputs(seed, f"gpu/amax4/{M}/{K}/{N}", M, K, N)
+        y = _gemm_w4a16_gpu(xb, qw, sc)
+        idx = qlin.gemm_w4a16_g128_argmax(to_dev_bits(xb, torch.bfloat16), to_dev(qw),
+                                          to_dev_bits(sc, torch.bfloat16))
+        ref = oracle.gemm_w4a16_g128(xb, qw, sc, K)
+    torch.cuda.synchronize()
+    return y, idx.cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("fmt,M,K,N", [("w8a8", 8, 512, 2000), ("w8a8", 96, 640, 3000),
+                                       ("w8a8", 1, 256, 136), ("w4a16", 8, 512, 2000),
+                                       ("w4a16", 64, 384, 1000)])
+def test_greedy_argmax_matches_gemm_and_oracle(fmt, M, K, N):
+    y, idx, ref = _argmax_case(fmt, M, K, N)
+    # the fused reduction sees the same bf16 values the plain call writes
+    assert np.array_equal(idx, oracle.argmax_bf16_rows(y))
+    # and picks a maximum of the oracle's output, up to the output tolerance:
+    # where the oracle's argmax differs, both columns' exact values lie within
+    # their error bounds (plus half an ulp each) of each other
+    want = oracle.argmax_bf16_rows(ref["y_bf16"])
+    rows = np.arange(M)
+    g, w = ref["y64"][rows, idx], ref["y64"][rows, want]
+    slack = ref["bound"][rows, idx] + ref["bound"][rows, want] + \
+        bf16_ulp(synth.bf16_values(ref["y_bf16"][rows, want]).astype(np.float64))
+    assert np.all((idx == want) | (np.abs(g - w) <= slack)), (idx, want)
+
+
+def test_greedy_argmax_ties_take_lowest_index():
+    M, K, N = 8, 256, 512
+    xb = synth.bf16_bits(np.abs(synth.bf16_values(
+        synth.activations(14, "gpu/amax/ties/x", M, K, "normal"))).astype(np.float32))
+    qa, sa = oracle.act_quant_i8(xb)
+    qwt = np.zeros((K, N), np.int8)
+    qwt[:, 300] = 1
+    qwt[:, 260] = 1                      # same 128-column tile: identical values
+    qw, _, _ = oracle.pack_gptq(qwt, 8)
+    sc = synth.f16_bits(np.full((K // 128, N), 0.01, np.float32))
+    idx = qlin.gemm_w8a8_gs128_argmax(to_dev(qa), to_dev(sa), to_dev(qw),
+                                      to_dev_bits(sc, torch.float16)).cpu().numpy()
+    assert idx.tolist() == [260] * M
+    # all outputs zero: the first column
+    qw0, _, _ = oracle.pack_gptq(np.zeros((K, N), np.int8), 8)
+    idx0 = qlin.gemm_w8a8_gs128_argmax(to_dev(qa), to_dev(sa), to_dev(qw0),
+                                       to_dev_bits(sc, torch.float16)).cpu().numpy()
+    assert idx0.tolist() == [0] * M

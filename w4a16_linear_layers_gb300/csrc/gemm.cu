@@ -71,7 +71,9 @@ constexpr uint32_t kSmemLimit = 232448; // 227 KB opt-in shared memory per block
 constexpr uint32_t kCtrlBytes = 1024;
 constexpr int kMaxStages = 16;           // weight ring slots
 constexpr int kMaxXSlots = 16;           // activation ring slots
-constexpr size_t kCounterBytes = 4096;   // int counters for up to 1024 blocks
+constexpr size_t kCounterBytes = 5120;   // int counters for up to 1024 blocks, then
+                                         // the argmax keys (kArgmaxKeysOffset)
+constexpr uint32_t kArgBytes = 4096;     // shared argmax keys: [4 lane quarters][128 tokens]
 constexpr int64_t kMinSteps = 8;          // minimum (tile, group) steps per block
 constexpr int kScaleChunk = 8;            // groups of scales per TMA load
 constexpr int kPreW = 3;                  // weight loads issued before the first activations
@@ -166,6 +168,7 @@ constexpr int kBufMax = 6;     // A buffers
 constexpr int kDBufMax = 16;   // D buffers
 
 struct KParams {
+  unsigned long long* amax_keys;   // greedy-argmax variant, else nullptr
   const float* s_a;
   void* out;
   int64_t M, N, G, F, W;
@@ -384,6 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sc_off = xi_off + static_cast<uint32_t>(C::kXiSlots) * C::kXiBytes;
   const uint16_t* scale_ring = reinterpret_cast<const uint16_t*>(smem + sc_off);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + sc_off + C::kScaleBytes);
+  unsigned long long* skeys =
+      reinterpret_cast<unsigned long long*>(smem + sc_off + C::kScaleBytes + kCtrlBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -737,7 +742,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool waited = false;
     PendingSplit pend[2];       // at most the first and the last tile of the range
     int npend = 0;
+    unsigned long long run_key[2] = {0ull, 0ull};   // greedy argmax: tokens lane, lane + 32
+    // Every final output value passes through here exactly once (full tiles
+    // at their segment end, split tiles in the last contributor).  All
+    // threads of each warp call it together.
     auto write_out = [&](int64_t tt, int64_t nn, const float* vals) {
+      if (p.amax_keys) {
+        // greedy argmax: key = order-preserving bits of the bf16 value << 32
+        // | ~n, so the largest key is the largest value at the lowest n; the
+        // warp's 32 features reduce by shuffles, the block's in shared memory
+        // The warp's 32 lanes hold 32 consecutive columns (nn - lane + 0..31),
+        // so within the warp a 32-bit key (value bits << 16 | 31 - lane)
+        // finds the same winner with one redux; lane 0 then forms the 64-bit
+        // key with the winning column.
+        if (tt * T + colbase >= M) return;            // no valid token in this half
+        const int64_t n0 = nn - lane;                  // column of lane 0
+#pragma unroll
+        for (int c = 0; c < C::kEpiCols; ++c) {
+          const int64_t m = tt * T + colbase + c;
+          uint32_t key = 0u;
+          if (nn < N && m < M) {
+            const float v = C::kW4 ? vals[c] : vals[c] * __ldg(p.s_a + m);
+            uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+            if (b == 0x8000u) b = 0u;   // -0 equals +0
+            const uint32_t ord = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+            key = (ord << 16) | static_cast<uint32_t>(31 - lane);
+          }
+          const uint32_t best = __reduce_max_sync(0xFFFFFFFFu, key);
+          if (best != 0u && lane == (c & 31)) {
+            // token c's running best lives in lane c % 32 of this warp
+            const uint32_t n_win = static_cast<uint32_t>(n0 + (31 - static_cast<int>(best & 0xFFFFu)));
+            const unsigned long long k64 = (static_cast<unsigned long long>(best >> 16) << 32) |
+                                           static_cast<unsigned long long>(~n_win);
+            if (k64 > run_key[c >> 5]) run_key[c >> 5] = k64;
+          }
+        }
+        return;
+      }
       if (nn >= N) return;
 #pragma unroll
       for (int c = 0; c < C::kEpiCols; ++c) {
@@ -863,6 +904,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           write_out(tt, (pend[k].tile - tt * F) * kTileF + r, acc);
         }
       }
+      if (p.amax_keys) {
+        // the block's best column per token (one token tile: M <= T): the
+        // four lane-quarter warps of each column half meet in shared memory
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int c = lane + 32 * i;
+          if (c < C::kEpiCols) skeys[(warp & 3) * kTileF + colbase + c] = run_key[i];
+        }
+        named_bar_sync(1, C::kEpiThreads);
+        if (et < T && et < M) {
+          unsigned long long k = skeys[et];
+#pragma unroll
+          for (int q = 1; q < 4; ++q) k = skeys[q * kTileF + et] > k ? skeys[q * kTileF + et] : k;
+          if (k != 0ull) {
+            if (!waited) grid_dep_wait();
+            atomicMax(&p.amax_keys[et], k);
+          }
+        }
+      }
     }
     __syncwarp();
   }
@@ -895,6 +955,18 @@ __global__ void __launch_bounds__(256) act_i8_to_f16_kernel(const int8_t* __rest
     biased_u8x4_to_f16x4(raw.w ^ 0x80808080u, o1.z, o1.w);
     reinterpret_cast<uint4*>(out)[2 * i] = o0;
     reinterpret_cast<uint4*>(out)[2 * i + 1] = o1;
+  }
+}
+
+// Greedy argmax: the column index encoded in each row's key.
+__global__ void __launch_bounds__(128) argmax_finalize_kernel(const unsigned long long* keys,
+                                                              int64_t M, int32_t* idx) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int64_t m = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (m < M) {
+    const unsigned long long k = keys[m];
+    idx[m] = k ? static_cast<int32_t>(~static_cast<uint32_t>(k & 0xFFFFFFFFull)) : -1;
   }
 }
 
@@ -992,7 +1064,7 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
   }
 
   const uint32_t fixed = 1024 + C::kXSlots * C::kABytes + C::kXiSlots * C::kXiBytes +
-                         C::kScaleBytes + kCtrlBytes;
+                         C::kScaleBytes + kCtrlBytes + kArgBytes;
   int stages = static_cast<int>((kSmemLimit - fixed) / C::kStageBytes);
   if (stages > kMaxStages) stages = kMaxStages;
   const uint32_t smem = fixed + static_cast<uint32_t>(stages) * C::kStageBytes;
@@ -1007,6 +1079,7 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
   if (attr_err != cudaSuccess) return attr_err;
 
   KParams kp;
+  kp.amax_keys = a.amax_keys;
   kp.s_a = a.s_a;
   kp.out = a.out;
   kp.M = a.M;
@@ -1036,6 +1109,12 @@ cudaError_t launch_mode(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStr
 
 }  // namespace
 
+cudaError_t launch_argmax_finalize(const unsigned long long* keys, int64_t M, int32_t* idx,
+                                   cudaStream_t stream) {
+  const unsigned blocks = static_cast<unsigned>((M + 127) / 128);
+  return launch_pdl(argmax_finalize_kernel, dim3(blocks), dim3(128), 0, stream, keys, M, idx);
+}
+
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
   GemmPlan p{};
   p.T = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 96 ? 96 : 128;
@@ -1047,8 +1126,8 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
   // blocks instead of splitting every tile across many of them.
   const int64_t by_work = (p.steps + kMinSteps - 1) / kMinSteps;
   p.ctas = by_work < sm_count ? by_work : sm_count;
-  if (p.ctas > static_cast<int64_t>(kCounterBytes / sizeof(int)))
-    p.ctas = static_cast<int64_t>(kCounterBytes / sizeof(int));
+  if (p.ctas > static_cast<int64_t>(kArgmaxKeysOffset / sizeof(int)))
+    p.ctas = static_cast<int64_t>(kArgmaxKeysOffset / sizeof(int));
   if (p.ctas < 1) p.ctas = 1;
   // One arrival counter per block: a tile split across blocks is counted on
   // the counter of its first contributing block, and a block is the first

@@ -100,6 +100,39 @@ qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const i
   return from_cuda(launch_gemm(a, plan, d->err_word, stream));
 }
 
+// Greedy-argmax variant of the two GEMMs: the keys live at a fixed offset in
+// the workspace's counter region; cleared, reduced by the GEMM, decoded.
+qlin_status_t run_argmax(GemmMode mode, const void* act, const float* s_a, const int32_t* qweight,
+                         const uint16_t* scales, int32_t* idx, int64_t M, int64_t N, int64_t K,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (act == nullptr || qweight == nullptr || scales == nullptr || idx == nullptr ||
+      (mode == GemmMode::kW8A8 && s_a == nullptr))
+    return QLIN_ERR_NULL;
+  qlin_status_t st = check_gemm_shape(M, N, K);
+  if (st != QLIN_OK) return st;
+  if (M > kArgmaxMaxRows) return QLIN_ERR_SHAPE;
+  if (!aligned16(act) || !aligned16(qweight) || !aligned16(scales) ||
+      (s_a && !aligned16(s_a)) || (workspace && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(idx) & 3u) != 0)
+    return QLIN_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  if (M == 0) return QLIN_OK;
+  const GemmPlan plan = plan_gemm(M, N, K, d->sm_count);
+  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return QLIN_ERR_WORKSPACE;
+  auto* keys = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) +
+                                                     kArgmaxKeysOffset);
+  if (cudaMemsetAsync(keys, 0, static_cast<size_t>(M) * sizeof(unsigned long long), stream) !=
+      cudaSuccess)
+    return QLIN_ERR_CUDA;
+  GemmArgs a{mode, act, s_a, qweight, scales, nullptr, M, N, K, workspace, workspace_bytes};
+  a.amax_keys = keys;
+  st = from_cuda(launch_gemm(a, plan, d->err_word, stream));
+  if (st != QLIN_OK) return st;
+  return from_cuda(launch_argmax_finalize(keys, M, idx, stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -131,6 +164,23 @@ qlin_status_t qlin_gemm_w4a16_g128(const uint16_t* x, const int32_t* qweight,
                                    qlin_stream_t stream) {
   return run_gemm(GemmMode::kW4A16, x, nullptr, qweight, scales, y, M, N, K, workspace,
                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_gemm_w8a8_gs128_argmax(const int8_t* q_a, const float* s_a,
+                                          const int32_t* qweight, const uint16_t* scales,
+                                          int64_t M, int64_t N, int64_t K, int32_t* argmax,
+                                          void* workspace, size_t workspace_bytes,
+                                          qlin_stream_t stream) {
+  return run_argmax(GemmMode::kW8A8, q_a, s_a, qweight, scales, argmax, M, N, K, workspace,
+                    workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_gemm_w4a16_g128_argmax(const uint16_t* x, const int32_t* qweight,
+                                          const uint16_t* scales, int64_t M, int64_t N, int64_t K,
+                                          int32_t* argmax, void* workspace,
+                                          size_t workspace_bytes, qlin_stream_t stream) {
+  return run_argmax(GemmMode::kW4A16, x, nullptr, qweight, scales, argmax, M, N, K, workspace,
+                    workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 qlin_status_t qlin_debug_group_partials_i8(const int8_t* q_a, const int32_t* qweight, int64_t M,

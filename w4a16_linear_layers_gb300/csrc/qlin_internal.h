@@ -40,7 +40,21 @@ struct GemmArgs {
   int64_t M, N, K;
   void* workspace;
   size_t workspace_bytes;
+  // Greedy-argmax variant: instead of writing y, reduce every output row to
+  // a 64-bit key (order-preserving bf16 bits << 32 | ~n) with atomicMax; the
+  // largest key is the largest value, lowest n on ties.  nullptr = write y.
+  unsigned long long* amax_keys = nullptr;
 };
+
+// Offset of the argmax keys (one per row, M <= 128) inside the fixed counter
+// region at the start of the workspace.
+constexpr size_t kArgmaxKeysOffset = 4096;
+constexpr int64_t kArgmaxMaxRows = 128;
+
+// idx[m] = the column index encoded in keys[m] (-1 if no key).  Programmatic
+// dependent launch: waits for the GEMM that produced the keys.
+cudaError_t launch_argmax_finalize(const unsigned long long* keys, int64_t M, int32_t* idx,
+                                   cudaStream_t stream);
 
 // Tiling plan for one GEMM call.
 struct GemmPlan {

@@ -35,6 +35,8 @@ EXPORTS = (
     "qlin_gemm_w8a8_gs128",
     "qlin_gemm_w8a8_gs128_noalloc",
     "qlin_gemm_w4a16_g128",
+    "qlin_gemm_w8a8_gs128_argmax",
+    "qlin_gemm_w4a16_g128_argmax",
     "qlin_pack_gptq",
     "qlin_workspace_bytes",
     "qlin_debug_group_partials_i8",
@@ -76,6 +78,8 @@ def load():
             "qlin_gemm_w8a8_gs128": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_gemm_w8a8_gs128_noalloc": ([P, P, P, P, I64, I64, I64, P, P], I),
             "qlin_gemm_w4a16_g128": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_gemm_w8a8_gs128_argmax": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_gemm_w4a16_g128_argmax": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_pack_gptq": ([P, I64, I64, I, P, P, P], I),
             "qlin_workspace_bytes": ([I64, I64, I64], SZ),
             "qlin_debug_group_partials_i8": ([P, P, I64, I64, I64, P, P, SZ, P], I),
@@ -239,6 +243,50 @@ def gemm_w4a16_g128(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor
     _check(load().qlin_gemm_w4a16_g128(_ptr(x), _ptr(qweight), _ptr(scales), M, N, K, _ptr(y),
                                        _ptr(ws), ws.numel(), _stream_handle(stream)))
     return y
+
+
+def gemm_w8a8_gs128_argmax(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
+                           scales: torch.Tensor, out: torch.Tensor | None = None,
+                           workspace=None, stream=None) -> torch.Tensor:
+    """Greedy token per row of the W8A8 GS128 linear (M <= 128): int32 [M],
+    the index of the largest bf16 output, lowest index on ties."""
+    _need(q_a, "q_a", torch.int8, 2)
+    _need(s_a, "s_a", torch.float32, 1)
+    _need(qweight, "qweight", torch.int32, 2)
+    _need(scales, "scales", torch.float16, 2)
+    M, K = q_a.shape
+    N = qweight.shape[1]
+    if qweight.shape[0] * 4 != K or scales.shape != (K // 128, N) or s_a.shape[0] != M:
+        raise ValueError("inconsistent W8A8 shapes")
+    if out is None:
+        out = torch.empty((M,), dtype=torch.int32, device=q_a.device)
+    _need(out, "out", torch.int32, 1)
+    ws = _workspace(workspace, M, N, K, q_a.device)
+    _check(load().qlin_gemm_w8a8_gs128_argmax(_ptr(q_a), _ptr(s_a), _ptr(qweight), _ptr(scales),
+                                              M, N, K, _ptr(out), _ptr(ws), ws.numel(),
+                                              _stream_handle(stream)))
+    return out
+
+
+def gemm_w4a16_g128_argmax(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                           out: torch.Tensor | None = None, workspace=None,
+                           stream=None) -> torch.Tensor:
+    """Greedy token per row of the W4A16 g128 linear (M <= 128)."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(qweight, "qweight", torch.int32, 2)
+    _need(scales, "scales", torch.bfloat16, 2)
+    M, K = x.shape
+    N = qweight.shape[1]
+    if qweight.shape[0] * 8 != K or scales.shape != (K // 128, N):
+        raise ValueError("inconsistent W4A16 shapes")
+    if out is None:
+        out = torch.empty((M,), dtype=torch.int32, device=x.device)
+    _need(out, "out", torch.int32, 1)
+    ws = _workspace(workspace, M, N, K, x.device)
+    _check(load().qlin_gemm_w4a16_g128_argmax(_ptr(x), _ptr(qweight), _ptr(scales), M, N, K,
+                                              _ptr(out), _ptr(ws), ws.numel(),
+                                              _stream_handle(stream)))
+    return out
 
 
 def pack_gptq(q: torch.Tensor, bits: int, qweight: torch.Tensor | None = None,
