@@ -17,6 +17,7 @@ patterns):
 * ``gemm_w4a16_g128(...)``            -> same dict
 * ``dequant_w4a16(qweight, scales, K, N)`` -> w bf16 bits [K,N]
 * ``argmax_bf16_rows(y_bits)``        -> int32 [M], greedy token per row
+* ``ingest_nk(packed_nk, scales_ng, K, N, bits)`` -> (qweight [K*bits/32,N], scales [K/128,N])
 """
 from __future__ import annotations
 
@@ -81,6 +82,8 @@ def _load():
             lib.orc_dequant_w4a16.restype = None
             lib.orc_argmax_bf16_rows.argtypes = [P, I, I, P]
             lib.orc_argmax_bf16_rows.restype = None
+            lib.orc_ingest_nk.argtypes = [P, P, I, I, ctypes.c_int, P, P]
+            lib.orc_ingest_nk.restype = None
             _lib = lib
     return _lib
 
@@ -222,3 +225,14 @@ def argmax_bf16_rows(y_bits) -> np.ndarray:
     idx = np.empty(M, np.int32)
     _load().orc_argmax_bf16_rows(_ptr(y), M, N, _ptr(idx))
     return idx
+
+
+def ingest_nk(packed_nk, scales_ng_bits, K: int, N: int, bits: int):
+    """compressed-tensors orientation (words [N, K*bits/32], scales [N, K/128])
+    -> the GEMMs' orientation (words [K*bits/32, N], scales [K/128, N])."""
+    pk = _c(packed_nk, np.int32)
+    sc = _c(scales_ng_bits, np.uint16)
+    qw = np.empty((K * bits // 32, N), np.int32)
+    so = np.empty((K // 128, N), np.uint16)
+    _load().orc_ingest_nk(_ptr(pk), _ptr(sc), K, N, bits, _ptr(qw), _ptr(so))
+    return qw, so

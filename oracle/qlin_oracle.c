@@ -304,3 +304,20 @@ void orc_argmax_bf16_rows(const uint16_t *y, int64_t M, int64_t N, int32_t *idx)
         idx[m] = (int32_t)best;
     }
 }
+
+/* Ingest of the compressed-tensors "pack-quantized" orientation
+ * ("Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card, property table, Format row: compressed-tensors
+ * pack-quantized, Marlin-compatible): the packed weight is stored per output
+ * row, word (n, kk) holding the same fields as the GPTQ word (kk, n) (field i
+ * = q[(32/bits) kk + i, n] + 2^(bits-1)), and the scales are [N, K/128].  The
+ * GEMMs read [K*bits/32, N] words and [K/128, N] scales: ingest is the
+ * transpose of both, bit for bit. */
+void orc_ingest_nk(const int32_t *packed_nk, const uint16_t *scales_ng, int64_t K, int64_t N,
+                   int bits, int32_t *qweight, uint16_t *scales)
+{
+    const int64_t R = K * bits / 32, G = K / GROUP;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t kk = 0; kk < R; ++kk) qweight[kk * N + n] = packed_nk[n * R + kk];
+        for (int64_t g = 0; g < G; ++g) scales[g * N + n] = scales_ng[n * G + g];
+    }
+}

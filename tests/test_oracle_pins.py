@@ -382,3 +382,42 @@ def test_argmax_rows_matches_numpy_first_max(oracle_lib):
     y = synth.bf16_bits(vals)
     want = np.argmax(synth.bf16_values(y).astype(np.float64), axis=1)
     assert np.array_equal(oracle_lib.argmax_bf16_rows(y), want.astype(np.int32))
+
+
+# ------------------------------------------------- [N, K/8] ingest (compressed-tensors)
+
+def _pack_rows_numpy(q: np.ndarray, bits: int) -> np.ndarray:
+    """Independent packer for the per-output-row orientation: word (n, kk)
+    field i = q[(32/bits) kk + i, n] + 2^(bits-1), least significant first."""
+    K, N = q.shape
+    per = 32 // bits
+    u = (q.astype(np.int64) + (1 << (bits - 1))).T.reshape(N, K // per, per)
+    words = np.zeros((N, K // per), np.int64)
+    for i in range(per):
+        words |= (u[:, :, i] & ((1 << bits) - 1)) << (bits * i)
+    return words.astype(np.uint32).view(np.int32)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_ingest_nk_matches_gptq_packing(oracle_lib, bits):
+    """The row-oriented words of q, ingested, equal the GPTQ words of q; the
+    scales are transposed unchanged."""
+    rng = np.random.default_rng(5 + bits)
+    lim = (1 << (bits - 1)) - 1
+    K, N = 256, 72
+    q = rng.integers(-lim, lim + 1, size=(K, N)).astype(np.int8)
+    scales_ng = rng.integers(0, 65536, size=(N, K // 128)).astype(np.uint16)
+    qw, sc = oracle_lib.ingest_nk(_pack_rows_numpy(q, bits), scales_ng, K, N, bits)
+    want, _, _ = oracle_lib.pack_gptq(q, bits)
+    assert np.array_equal(qw, want)
+    assert np.array_equal(sc, scales_ng.T)
+
+
+def test_ingest_nk_hand_word(oracle_lib):
+    """One 4-bit column: q[0..7, 0] = -8..-1 -> nibbles 0..7 -> 0x76543210."""
+    q = np.zeros((128, 1), np.int8)
+    q[:8, 0] = np.arange(-8, 0)
+    packed = _pack_rows_numpy(q, 4)
+    assert packed[0, 0] == 0x76543210
+    qw, _ = oracle_lib.ingest_nk(packed, np.zeros((1, 1), np.uint16), 128, 1, 4)
+    assert qw[0, 0] == 0x76543210
