@@ -8,7 +8,10 @@
  *   2. a W8A8 GEMM against GPTQ-packed symmetric INT8 weights with one fp16
  *      scale per 128-wide K group (GS128),
  *   3. the W4A16 g128 symmetric weight-only GEMM with bf16 activations,
- *   4. the GPTQ packer that produces the weight format of 2 and 3.
+ *   4. the GPTQ packer that produces the weight format of 2 and 3,
+ *   5. the vocabulary head with fused greedy argmax (2 or 3 reduced to the
+ *      largest output per row),
+ *   6. the ingest of the compressed-tensors per-output-row packed orientation.
  *
  * Format (all calls): GPTQ qweight / qzeros / scales, no g_idx,
  * desc_act = false, symmetric, groups of exactly 128 contiguous K
@@ -32,7 +35,7 @@
  *    N = output features.  K must be a positive multiple of 128, N a positive
  *    multiple of 8, M >= 0 (M == 0 is a no-op), and M, N, K <= 2^31 - 1.
  *  - Alignment: every pointer must be 16-byte aligned (the kernels move data
- *    with TMA and 16-byte vector accesses).
+ *    with TMA and 16-byte vector accesses), unless a call states otherwise.
  *  - The calls run only on an sm_103 GPU (GB300); elsewhere they return
  *    QLIN_ERR_DEVICE.
  */
@@ -220,6 +223,27 @@ qlin_status_t qlin_gemm_w4a16_g128_argmax(const uint16_t *x, const int32_t *qwei
  */
 qlin_status_t qlin_pack_gptq(const int8_t *q, int64_t K, int64_t N, int bits,
                              int32_t *qweight, int32_t *qzeros, qlin_stream_t stream);
+
+/*
+ * Ingest of the compressed-tensors "pack-quantized" orientation, the native
+ * format of the "Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card (property
+ * table, Format row).  There the packed weight is stored per output row:
+ * word (n, kk) holds the same fields as GPTQ word (kk, n) (field i =
+ * q_w[(32/bits) kk + i, n] + 2^(bits-1), field 0 least significant), and the
+ * scales are [N, K/128].  This call transposes both, bit for bit, into the
+ * orientation the GEMMs read (offline step; not on the timed path).
+ *
+ *   packed_nk  int32 [N, K*bits/32]   device, 4-byte aligned
+ *   scales_ng  16-bit [N, K/128]      device, 2-byte aligned (bf16 or fp16 bits)
+ *   bits       4 or 8
+ *   qweight    int32 [K*bits/32, N]   output, device, 16-byte aligned
+ *   scales     16-bit [K/128, N]      output, device, 16-byte aligned
+ *
+ * K must be a multiple of 128.  Asynchronous on `stream`.
+ */
+qlin_status_t qlin_ingest_nk(const int32_t *packed_nk, const uint16_t *scales_ng, int64_t K,
+                             int64_t N, int bits, int32_t *qweight, uint16_t *scales,
+                             qlin_stream_t stream);
 
 /*
  * Bytes of workspace the two GEMMs need for (M, N, K) on the current device

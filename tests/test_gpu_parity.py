@@ -356,3 +356,39 @@ def test_greedy_argmax_ties_take_lowest_index():
     idx0 = qlin.gemm_w8a8_gs128_argmax(to_dev(qa), to_dev(sa), to_dev(qw0),
                                        to_dev_bits(sc, torch.float16)).cpu().numpy()
     assert idx0.tolist() == [0] * M
+
+
+# ---------------------------------------- [N, K/8] ingest (compressed-tensors)
+
+def _pack_rows(q: np.ndarray, bits: int) -> np.ndarray:
+    """Per-output-row packing of q (the compressed-tensors orientation), from
+    the oracle's GPTQ words: word (n, kk) = GPTQ word (kk, n)."""
+    qw, _, _ = oracle.pack_gptq(q, bits)
+    return np.ascontiguousarray(qw.T)
+
+
+@pytest.mark.parametrize("bits,K,N", [(4, 384, 72), (4, 5120, 1000), (8, 256, 40), (8, 1280, 2056)])
+def test_ingest_nk_bit_exact(bits, K, N):
+    rng = np.random.default_rng(bits * 7 + N)
+    lim = (1 << (bits - 1)) - 1
+    q = rng.integers(-lim, lim + 1, size=(K, N)).astype(np.int8)
+    scales_ng = rng.integers(0, 65536, size=(N, K // 128)).astype(np.uint16)
+    packed = _pack_rows(q, bits)
+    want_w, want_s = oracle.ingest_nk(packed, scales_ng, K, N, bits)
+    qw, sc = qlin.ingest_nk(to_dev(packed), to_dev_bits(scales_ng, torch.bfloat16), K, bits)
+    torch.cuda.synchronize()
+    assert np.array_equal(qw.cpu().numpy(), want_w)
+    assert np.array_equal(from_dev_bits(sc), want_s)
+
+
+def test_w4a16_from_ingested_weights_matches_oracle():
+    """End to end: compressed-tensors weights ingested on the device, then the
+    W4A16 GEMM, against the oracle on the GPTQ-oriented words."""
+    M, K, N = 17, 640, 264
+    xb, _, qw, sb = _w4a16_inputs(15, "gpu/ingest/w4", M, K, N)
+    packed = np.ascontiguousarray(qw.T)
+    sb_ng = np.ascontiguousarray(sb.T)
+    qw_d, sb_d = qlin.ingest_nk(to_dev(packed), to_dev_bits(sb_ng, torch.bfloat16), K, 4)
+    y = qlin.gemm_w4a16_g128(to_dev_bits(xb, torch.bfloat16), qw_d, sb_d)
+    torch.cuda.synchronize()
+    compare_linear(from_dev_bits(y), oracle.gemm_w4a16_g128(xb, qw, sb, K), "ingested w4a16")

@@ -1,4 +1,5 @@
-// pack.cu -- GPTQ packer (offline step) and the bounded-wait test kernel.
+// pack.cu -- GPTQ packer and the compressed-tensors ingest (offline steps),
+// and the bounded-wait test kernel.
 //
 // Packing follows the GPTQ format of the "Flint-DFlash2-GPTQ-INT8-PTQR" card
 // (qweight/qzeros, symmetric, INT8) and the INT32-packed 4-bit weights of the
@@ -63,7 +64,45 @@ unsigned grid_for(int64_t n, int threads) {
   return static_cast<unsigned>(blocks);
 }
 
+// dst[c][r] = src[r][c] through a 32 x 33 shared tile (both sides coalesced).
+template <typename U>
+__global__ void __launch_bounds__(256) transpose_kernel(const U* __restrict__ src, int64_t R,
+                                                        int64_t C, U* __restrict__ dst) {
+  __shared__ U tile[32][33];
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    if (r < R && c < C) tile[i][threadIdx.x] = src[r * C + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (c < C && r < R) dst[c * R + r] = tile[threadIdx.x][i];
+  }
+}
+
+template <typename U>
+cudaError_t transpose(const U* src, int64_t R, int64_t C, U* dst, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((C + 31) / 32), static_cast<unsigned>((R + 31) / 32));
+  transpose_kernel<U><<<grid, dim3(32, 8), 0, stream>>>(src, R, C, dst);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+// Ingest of the compressed-tensors "pack-quantized" orientation
+// ("Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card, property table, Format row):
+// word (n, kk) of the per-output-row packing holds the same fields as GPTQ
+// word (kk, n), and the scales are [N, K/128]; the GEMMs read [K*bits/32, N]
+// words and [K/128, N] scales, so both are transposed bit for bit.
+cudaError_t launch_ingest_nk(const int32_t* packed_nk, const uint16_t* scales_ng, int64_t K,
+                             int64_t N, int bits, int32_t* qweight, uint16_t* scales,
+                             cudaStream_t stream) {
+  cudaError_t e = transpose<int32_t>(packed_nk, N, K * bits / 32, qweight, stream);
+  if (e != cudaSuccess) return e;
+  return transpose<uint16_t>(scales_ng, N, K / kGroup, scales, stream);
+}
 
 cudaError_t launch_pack(const int8_t* q, int64_t K, int64_t N, int bits, int32_t* qweight,
                         int32_t* qzeros, int* err, cudaStream_t stream) {

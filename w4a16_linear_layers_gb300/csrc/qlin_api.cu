@@ -190,6 +190,24 @@ qlin_status_t qlin_debug_group_partials_i8(const int8_t* q_a, const int32_t* qwe
                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+qlin_status_t qlin_ingest_nk(const int32_t* packed_nk, const uint16_t* scales_ng, int64_t K,
+                             int64_t N, int bits, int32_t* qweight, uint16_t* scales,
+                             qlin_stream_t stream) {
+  if (packed_nk == nullptr || scales_ng == nullptr || qweight == nullptr || scales == nullptr)
+    return QLIN_ERR_NULL;
+  if (bits != 4 && bits != 8) return QLIN_ERR_BITS;
+  if (N < 1 || N > kMaxDim || K < kGroup || K > kMaxDim || (K % kGroup) != 0)
+    return QLIN_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(packed_nk) & 3u) || (reinterpret_cast<uintptr_t>(scales_ng) & 1u) ||
+      !aligned16(qweight) || !aligned16(scales))
+    return QLIN_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  qlin_status_t st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  return from_cuda(launch_ingest_nk(packed_nk, scales_ng, K, N, bits, qweight, scales,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
 qlin_status_t qlin_pack_gptq(const int8_t* q, int64_t K, int64_t N, int bits, int32_t* qweight,
                              int32_t* qzeros, qlin_stream_t stream) {
   if (q == nullptr || qweight == nullptr) return QLIN_ERR_NULL;

@@ -27,6 +27,10 @@ cudaError_t launch_pack(const int8_t* q, int64_t K, int64_t N, int bits, int32_t
 
 cudaError_t launch_wait_timeout(int64_t limit_ns, int* err, cudaStream_t stream);
 
+cudaError_t launch_ingest_nk(const int32_t* packed_nk, const uint16_t* scales_ng, int64_t K,
+                             int64_t N, int bits, int32_t* qweight, uint16_t* scales,
+                             cudaStream_t stream);
+
 // GEMM problem description passed from the API to the launcher.
 enum class GemmMode : int { kW8A8 = 0, kW8A8Partials = 1, kW4A16 = 2 };
 

@@ -38,6 +38,7 @@ EXPORTS = (
     "qlin_gemm_w8a8_gs128_argmax",
     "qlin_gemm_w4a16_g128_argmax",
     "qlin_pack_gptq",
+    "qlin_ingest_nk",
     "qlin_workspace_bytes",
     "qlin_debug_group_partials_i8",
     "qlin_debug_wait_timeout",
@@ -81,6 +82,7 @@ def load():
             "qlin_gemm_w8a8_gs128_argmax": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_gemm_w4a16_g128_argmax": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_pack_gptq": ([P, I64, I64, I, P, P, P], I),
+            "qlin_ingest_nk": ([P, P, I64, I64, I, P, P, P], I),
             "qlin_workspace_bytes": ([I64, I64, I64], SZ),
             "qlin_debug_group_partials_i8": ([P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_debug_wait_timeout": ([I64, P], I),
@@ -287,6 +289,24 @@ def gemm_w4a16_g128_argmax(x: torch.Tensor, qweight: torch.Tensor, scales: torch
                                               _ptr(out), _ptr(ws), ws.numel(),
                                               _stream_handle(stream)))
     return out
+
+
+def ingest_nk(packed_nk: torch.Tensor, scales_ng: torch.Tensor, K: int, bits: int,
+              stream=None):
+    """compressed-tensors orientation (words int32 [N, K*bits/32], 16-bit scales
+    [N, K/128]) -> the GEMMs' orientation (qweight [K*bits/32, N], scales
+    [K/128, N], same dtype as scales_ng)."""
+    _need(packed_nk, "packed_nk", torch.int32, 2)
+    if scales_ng.dtype not in (torch.float16, torch.bfloat16) or scales_ng.dim() != 2:
+        raise ValueError("scales_ng must be a 2-D fp16 or bf16 tensor")
+    N = packed_nk.shape[0]
+    if packed_nk.shape[1] * 32 != K * bits or scales_ng.shape != (N, K // 128):
+        raise ValueError("inconsistent ingest shapes")
+    qweight = torch.empty((K * bits // 32, N), dtype=torch.int32, device=packed_nk.device)
+    scales = torch.empty((K // 128, N), dtype=scales_ng.dtype, device=packed_nk.device)
+    _check(load().qlin_ingest_nk(_ptr(packed_nk.contiguous()), _ptr(scales_ng.contiguous()), K, N,
+                                 bits, _ptr(qweight), _ptr(scales), _stream_handle(stream)))
+    return qweight, scales
 
 
 def pack_gptq(q: torch.Tensor, bits: int, qweight: torch.Tensor | None = None,
