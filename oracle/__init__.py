@@ -15,6 +15,7 @@ patterns):
 * ``group_partials_i8(qa, qweight, K)``-> P int32 [G,M,N]
 * ``gemm_w8a8_gs128(...)``            -> dict of y_bf16 / y_f32 / y64 / bound
 * ``gemm_w4a16_g128(...)``            -> same dict
+* ``gemm_w8a16(..., group_size)``     -> same dict (int8 weight-only; g32, g128 or per channel)
 * ``dequant_w4a16(qweight, scales, K, N)`` -> w bf16 bits [K,N]
 * ``argmax_bf16_rows(y_bits)``        -> int32 [M], greedy token per row
 * ``ingest_nk(packed_nk, scales_ng, K, N, bits)`` -> (qweight [K*bits/32,N], scales [K/128,N])
@@ -84,6 +85,8 @@ def _load():
             lib.orc_argmax_bf16_rows.restype = None
             lib.orc_ingest_nk.argtypes = [P, P, I, I, ctypes.c_int, P, P]
             lib.orc_ingest_nk.restype = None
+            lib.orc_gemm_w8a16.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, P, P]
+            lib.orc_gemm_w8a16.restype = None
             _lib = lib
     return _lib
 
@@ -206,6 +209,26 @@ def gemm_w4a16_g128(x_bits, qweight, scales_bf16_bits, K, rows=None, cols=None):
                                 _ptr(r), r.size, _ptr(c), c.size,
                                 _ptr(out["y_bf16"]), _ptr(out["y_f32"]),
                                 _ptr(out["y64"]), _ptr(out["bound"]))
+    return out
+
+
+def gemm_w8a16(x_bits, qweight, scales_bf16_bits, K, group_size, rows=None, cols=None):
+    """W8A16 weight-only int8 linear on a sub-grid of outputs.
+
+    x bf16 bits [M,K], qweight int32 [K/4,N] (8-bit GPTQ words), scales bf16
+    bits [K/group_size, N], or [1, N] for group_size 0 (one scale per column)."""
+    x = _c(x_bits, np.uint16)
+    qw = _c(qweight, np.int32)
+    sc = _c(scales_bf16_bits, np.uint16)
+    M = x.shape[0]
+    N = qw.shape[1]
+    r = _index(rows, M)
+    c = _index(cols, N)
+    out = _outputs(r.size, c.size)
+    _load().orc_gemm_w8a16(_ptr(x), _ptr(qw), _ptr(sc), M, N, K, int(group_size),
+                           _ptr(r), r.size, _ptr(c), c.size,
+                           _ptr(out["y_bf16"]), _ptr(out["y_f32"]),
+                           _ptr(out["y64"]), _ptr(out["bound"]))
     return out
 
 

@@ -321,3 +321,42 @@ void orc_ingest_nk(const int32_t *packed_nk, const uint16_t *scales_ng, int64_t 
         for (int64_t g = 0; g < G; ++g) scales[g * N + n] = scales_ng[n * G + g];
     }
 }
+
+/* W8A16 weight-only int8 linear ("Qwen3.5-4B-DFlash-W8A16" card: a
+ * weight-only int8 drafter made by round-to-nearest on the weights; "DFlash2
+ * decoding" recipe page: int8 drafter projections with group-32 scales).
+ * Read like W4A16: w[k, n] = bf16(q[k, n] * s[k / gs, n]) (one rounding of an
+ * exact product), y = bf16(sum_k x[m, k] * w[k, n]) accumulated in fp32 over
+ * k ascending.  q comes from the 8-bit GPTQ words ([K/4, N], byte = q + 128);
+ * scales are bf16 [K/gs, N], with gs = 0 meaning one scale per output column
+ * (scales [1, N]).  y64 / bound as for W4A16. */
+void orc_gemm_w8a16(const uint16_t *x, const int32_t *qweight, const uint16_t *scales_bf16,
+                    int64_t M, int64_t N, int64_t K, int64_t gs,
+                    const int64_t *rows, int64_t nrows, const int64_t *cols, int64_t ncols,
+                    uint16_t *y_bf16, float *y_f32, double *y64, double *bound)
+{
+    (void)M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t m = rows[r];
+        for (int64_t c = 0; c < ncols; ++c) {
+            const int64_t n = cols[c];
+            float acc = 0.0f;
+            double exact = 0.0, magnitude = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const int64_t g = gs > 0 ? k / gs : 0;
+                const float s = orc_bf16_to_f32(scales_bf16[g * N + n]);
+                const float w = orc_bf16_to_f32(orc_f32_to_bf16((float)weight_at(qweight, N, 8, k, n) * s));
+                const float xv = orc_bf16_to_f32(x[m * K + k]);
+                const float prod = xv * w;
+                acc = acc + prod;
+                exact += (double)xv * (double)w;
+                magnitude += fabs((double)xv * (double)w);
+            }
+            const int64_t o = r * ncols + c;
+            y_f32[o] = acc;
+            y_bf16[o] = orc_f32_to_bf16(acc);
+            y64[o] = exact;
+            bound[o] = (double)(K + 2) * ldexp(1.0, -23) * magnitude;
+        }
+    }
+}

@@ -421,3 +421,48 @@ def test_ingest_nk_hand_word(oracle_lib):
     assert packed[0, 0] == 0x76543210
     qw, _ = oracle_lib.ingest_nk(packed, np.zeros((1, 1), np.uint16), 128, 1, 4)
     assert qw[0, 0] == 0x76543210
+
+
+# ------------------------------------------------------ W8A16 (int8 weight-only)
+
+def _expand_scales(sb, K, gs):
+    v = synth.bf16_values(sb)
+    return np.repeat(v, K, axis=0) if gs == 0 else np.repeat(v, gs, axis=0)
+
+
+@pytest.mark.parametrize("gs", [32, 128, 0])
+def test_w8a16_identity_probe_bit_exact(oracle_lib, gs):
+    """Identity probe: y = bf16(q * s) exactly (library rounding of the exact
+    fp32 product), for group-32, group-128 and per-column scales."""
+    K, N = 256, 40
+    qwt, sb = synth.w8a16_weights(8, f"pin/probe8/{gs}", K, N, gs)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    xb = bf16_of(np.eye(K, dtype=np.float32))
+    out = oracle_lib.gemm_w8a16(xb, qw, sb, K, gs)
+    want = bf16_of(qwt.astype(np.float32) * _expand_scales(sb, K, gs))
+    assert np.array_equal(out["y_bf16"], want)
+
+
+def test_w8a16_unit_scales_integer(oracle_lib):
+    M, K, N = 4, 512, 9
+    x_int = synth.randint(12, "pin/w8unit/x", (M, K), -3, 3).astype(np.float32)
+    qwt = synth.randint(12, "pin/w8unit/w", (K, N), -127, 127)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    ones = np.full((K // 32, N), 0x3F80, np.uint16)       # bf16 1.0
+    out = oracle_lib.gemm_w8a16(bf16_of(x_int), qw, ones, K, 32)
+    ref = x_int.astype(np.int64) @ qwt.astype(np.int64)
+    assert np.array_equal(out["y_f32"], ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("gs", [32, 0])
+def test_w8a16_fp64_invariant(oracle_lib, gs):
+    M, K, N = 6, 1152, 50
+    xb = synth.activations(13, f"pin/w8f64/{gs}/x", M, K, "normal")
+    qwt, sb = synth.w8a16_weights(13, f"pin/w8f64/{gs}/w", K, N, gs)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    out = oracle_lib.gemm_w8a16(xb, qw, sb, K, gs)
+    w = synth.bf16_values(bf16_of(qwt.astype(np.float32) * _expand_scales(sb, K, gs))).astype(np.float64)
+    ref = synth.bf16_values(xb).astype(np.float64) @ w
+    assert np.allclose(out["y64"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert np.all(np.abs(out["y_f32"].astype(np.float64) - out["y64"]) <= out["bound"])
+    assert np.array_equal(out["y_bf16"], bf16_of(out["y_f32"]))

@@ -204,6 +204,17 @@ def w4a16_weights(seed: int, name: str, K: int, N: int, scale_lo: float = 1e-3,
     return q, s
 
 
+def w8a16_weights(seed: int, name: str, K: int, N: int, group_size: int,
+                  scale_lo: float = 1e-3, scale_hi: float = 1e-2):
+    """Symmetric int8 weights q [K, N] uniform on [-127, 127] and bf16 scales
+    log-uniform on [scale_lo, scale_hi] (bits): [K/group_size, N], or [1, N]
+    (one scale per output column) for group_size 0."""
+    q = randint(seed, name + "/qw", (K, N), -127, 127, np.int8)
+    rows = 1 if group_size == 0 else K // group_size
+    s = bf16_bits(log_uniform(seed, name + "/sw", (rows, N), scale_lo, scale_hi))
+    return q, s
+
+
 # The drafter layer's seven projections (hidden 5120, intermediate 17408,
 # 32 query heads and 8 key/value heads of dimension 128) and the target-hidden
 # projection fc (5 x 5120 -> 5120).  (name, K, N, activation kind)
