@@ -7,7 +7,8 @@
  *   1. dynamic per-token symmetric INT8 activation quantization,
  *   2. a W8A8 GEMM against GPTQ-packed symmetric INT8 weights with one fp16
  *      scale per 128-wide K group (GS128),
- *   3. the W4A16 g128 symmetric weight-only GEMM with bf16 activations,
+ *   3. the W4A16 g128 symmetric weight-only GEMM with bf16 activations, and
+ *      its int8 sibling W8A16 (group-32, group-128 or per-column scales),
  *   4. the GPTQ packer that produces the weight format of 2 and 3,
  *   5. the vocabulary head with fused greedy argmax (2 or 3 reduced to the
  *      largest output per row),
@@ -172,6 +173,29 @@ qlin_status_t qlin_gemm_w4a16_g128(const uint16_t *x, const int32_t *qweight,
                                    const uint16_t *scales, int64_t M, int64_t N,
                                    int64_t K, uint16_t *y, void *workspace,
                                    size_t workspace_bytes, qlin_stream_t stream);
+
+/*
+ * W8A16 int8 weight-only linear, bf16 activations:
+ *   w[k,n] = bf16( q_w[k,n] * s[k / group_size, n] ),   y = bf16( sum_k x[m,k] * w[k,n] )
+ * accumulated in fp32 (one rounding of each exact product q * s).
+ *
+ * Passages: "Qwen3.5-4B-DFlash-W8A16" card (a weight-only int8 drafter, RTN
+ * on the weights, bf16 activations); "DFlash2 decoding" recipe page (int8
+ * drafter projections with group-32 scales).
+ *
+ *   x           bf16  [M, K]             activations
+ *   qweight     int32 [K/4, N]           8-bit GPTQ words as for the W8A8 GEMM
+ *                                        (byte i of word (kk, n) = q_w[4kk+i, n] + 128)
+ *   scales      bf16  [K/group_size, N]  group scales, or [1, N] for group_size 0
+ *   group_size  32, 128, or 0 (one scale per output column)
+ *   y           bf16  [M, N]             output
+ *   workspace / workspace_bytes          as for qlin_gemm_w8a8_gs128
+ *
+ * Any other group_size returns QLIN_ERR_SHAPE.
+ */
+qlin_status_t qlin_gemm_w8a16(const uint16_t *x, const int32_t *qweight, const uint16_t *scales,
+                              int64_t M, int64_t N, int64_t K, int group_size, uint16_t *y,
+                              void *workspace, size_t workspace_bytes, qlin_stream_t stream);
 
 /*
  * Vocabulary head with fused greedy argmax: the same linear as

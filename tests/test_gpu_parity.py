@@ -392,3 +392,43 @@ def test_w4a16_from_ingested_weights_matches_oracle():
     y = qlin.gemm_w4a16_g128(to_dev_bits(xb, torch.bfloat16), qw_d, sb_d)
     torch.cuda.synchronize()
     compare_linear(from_dev_bits(y), oracle.gemm_w4a16_g128(xb, qw, sb, K), "ingested w4a16")
+
+
+# ------------------------------------------------------ W8A16 (int8 weight-only)
+
+def _w8a16_inputs(seed, name, M, K, N, gs):
+    xb = synth.activations(seed, name + "/x", M, K, "normal")
+    qwt, sb = synth.w8a16_weights(seed, name + "/w", K, N, gs)
+    qw, _, _ = oracle.pack_gptq(qwt, 8)
+    return xb, qw, sb
+
+
+@pytest.mark.parametrize("gs", [32, 128, 0])
+@pytest.mark.parametrize("M,K,N", [(1, 128, 128), (8, 5120, 1024), (17, 640, 264), (64, 1280, 384),
+                                   (96, 384, 136), (130, 256, 200)])
+def test_w8a16_matches_oracle(M, K, N, gs):
+    xb, qw, sb = _w8a16_inputs(16, f"gpu/w8a16/{M}/{K}/{N}/{gs}", M, K, N, gs)
+    y = qlin.gemm_w8a16(to_dev_bits(xb, torch.bfloat16), to_dev(qw), to_dev_bits(sb, torch.bfloat16), gs)
+    torch.cuda.synchronize()
+    compare_linear(from_dev_bits(y), oracle.gemm_w8a16(xb, qw, sb, K, gs), f"w8a16 g{gs} {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("gs", [32, 0])
+def test_w8a16_identity_probe_bit_exact(gs):
+    """Feeding I_K recovers w = bf16(q * s) bit for bit (one nonzero product
+    per output, so any summation order gives the same value)."""
+    K, N = 256, 384
+    xb = synth.bf16_bits(np.eye(K, dtype=np.float32))
+    _, qw, sb = _w8a16_inputs(17, f"gpu/w8a16/probe/{gs}", K, K, N, gs)
+    y = qlin.gemm_w8a16(to_dev_bits(xb, torch.bfloat16), to_dev(qw), to_dev_bits(sb, torch.bfloat16), gs)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev_bits(y), oracle.gemm_w8a16(xb, qw, sb, K, gs)["y_bf16"])
+
+
+def test_w8a16_rejects_other_group_sizes():
+    x = torch.zeros((8, 256), dtype=torch.bfloat16, device="cuda")
+    qw = torch.zeros((64, 128), dtype=torch.int32, device="cuda")
+    sc = torch.zeros((4, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(qlin.QlinError) as e:
+        qlin.gemm_w8a16(x, qw, sc, 64)
+    assert e.value.status == qlin.QLIN_ERR_SHAPE

@@ -81,10 +81,14 @@ constexpr int kPreW = 3;                  // weight loads issued before the firs
 constexpr int kModeW8A8 = 0;
 constexpr int kModeP = 1;     // W8A8 pipeline, exports the group partials
 constexpr int kModeW4 = 2;
+constexpr int kModeW8A16 = 3;   // int8 weight-only: group-32, group-128 or per-column scales
 
 template <int kMode, int T>
 struct Cfg {
-  static constexpr bool kW4 = kMode == kModeW4;
+  // weight-only formats (W4A16, W8A16): bf16 tokens, scales applied by the
+  // converters, the whole K accumulated in TMEM
+  static constexpr bool kWO = kMode == kModeW4 || kMode == kModeW8A16;
+  static constexpr bool kInt4 = kMode == kModeW4;
   // warps 0..3: control (0 weight TMA, 1 TMEM owner + MMA issuer, 2 activation
   //             and scale TMA, 3 MMA issuer)
   // warps 4..11: converters, two groups of four taking alternate steps (each
@@ -98,7 +102,7 @@ struct Cfg {
   static constexpr int kEpiWarps = 8;
   static constexpr int kConvThreads = 32 * kConvWarps;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
-  static constexpr int kWordRows = kW4 ? 16 : 32;           // int32 rows per group
+  static constexpr int kWordRows = kInt4 ? 16 : 32;         // int32 rows per group
   static constexpr uint32_t kWBytes = kWordRows * kTileF * 4;
   static constexpr uint32_t kABytes = 2u * T * 128u;         // two 64-wide 16-bit halves
   // Weights and activations travel in rings of their own, so neither stream
@@ -117,31 +121,31 @@ struct Cfg {
   static constexpr uint32_t kStageBytes = kWBytes;
   static constexpr uint32_t kXiBytes = static_cast<uint32_t>(T) * 128u;   // int8 tile
   static constexpr int kXiRaw = static_cast<int>(32768u / kXiBytes);
-  static constexpr bool kXConv = !kW4 && T <= 64;
+  static constexpr bool kXConv = !kWO && T <= 64;
   static constexpr int kXiSlots = !kXConv ? 0 : (kXiRaw < 4 ? 4 : (kXiRaw > kMaxXSlots ? kMaxXSlots : kXiRaw));
   static constexpr int kXSlotsRaw = static_cast<int>(65536u / kABytes);
   static constexpr int kXSlotsW4 = kXSlotsRaw < 4 ? 4 : (kXSlotsRaw > kMaxXSlots ? kMaxXSlots : kXSlotsRaw);
   static constexpr int kIssuers = 2;
   // W4A16 accumulates a whole segment in TMEM: one accumulator per issuer
   // and segment buffer (two segment buffers while they fit).
-  static constexpr int kSegBufs = kW4 ? (T <= 96 ? 2 : 1) : 0;
-  static constexpr int kW4DCols = kW4 ? kSegBufs * kIssuers * T : 0;
+  static constexpr int kSegBufs = kWO ? (T <= 96 ? 2 : 1) : 0;
+  static constexpr int kW4DCols = kWO ? kSegBufs * kIssuers * T : 0;
   // A (64 TMEM columns) and, for W8A8, D (T columns) buffers in flight
   // between the converters, the MMA issuers and the epilogue.
   // W8A8 sizes the A buffers (converter -> MMA) and the D buffers (MMA ->
   // epilogue) separately: the epilogue loop (MMA completion, TMEM drain,
   // release) is the long one, so small token tiles get many D buffers.
-  static constexpr int kNumBufRaw = kW4 ? (512 - kW4DCols) / 64 : (T <= 64 ? 4 : 2);
+  static constexpr int kNumBufRaw = kWO ? (512 - kW4DCols) / 64 : (T <= 64 ? 4 : 2);
   static constexpr int kNumBuf = kNumBufRaw < 6 ? kNumBufRaw : 6;
-  static constexpr int kNumDFit = kW4 ? 1 : (512 - 64 * kNumBuf) / T;
+  static constexpr int kNumDFit = kWO ? 1 : (512 - 64 * kNumBuf) / T;
   static constexpr int kNumDRaw = kNumDFit < 16 ? kNumDFit : 16;
   // ND - NA even: see the waits of the converters
-  static constexpr int kNumD = kW4 ? 1 : kNumDRaw - ((kNumDRaw - kNumBuf) & 1);
+  static constexpr int kNumD = kWO ? 1 : kNumDRaw - ((kNumDRaw - kNumBuf) & 1);
   // W8A8 commits once per step, on the step's D buffer: that completion also
   // frees the step's A buffer and fp16 operand slot (slot i pairs with A
   // buffer i), which the converters wait for before they refill both.
   static constexpr int kXSlots = kXConv ? kNumBuf : kXSlotsW4;
-  static_assert(kW4 || (kNumD >= kNumBuf && (kNumD - kNumBuf) % 2 == 0),
+  static_assert(kWO || (kNumD >= kNumBuf && (kNumD - kNumBuf) % 2 == 0),
                 "one commit per step needs ND >= NA with ND - NA even");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColA = 0;
@@ -154,13 +158,15 @@ struct Cfg {
   // (W4A16).
   static constexpr bool kScales = kMode != kModeP;
   static constexpr int kScaleSlots = 4;
-  static constexpr uint32_t kScaleSlotBytes = kScaleChunk * 256u;
+  // W8A16 group-32 scales bring 4 rows per 128-wide group
+  static constexpr uint32_t kScaleRowsMax = kMode == kModeW8A16 ? 4 * kScaleChunk : kScaleChunk;
+  static constexpr uint32_t kScaleSlotBytes = kScaleRowsMax * 256u;
   static constexpr uint32_t kScaleBytes = kScales ? kScaleSlots * kScaleSlotBytes : 0u;
   static_assert(T % 16 == 0 && T >= 16 && T <= 128, "token tile");
   static_assert(kEpiCols % 8 == 0, "epilogue columns");
   static_assert(kNumBuf >= 2, "double buffering at least");
-  static_assert(kColD + (kW4 ? kW4DCols : kNumD * T) <= kTmemCols, "TMEM budget");
-  static_assert(kW4 || kNumD >= 2, "double buffering at least");
+  static_assert(kColD + (kWO ? kW4DCols : kNumD * T) <= kTmemCols, "TMEM budget");
+  static_assert(kWO || kNumD >= 2, "double buffering at least");
   static_assert(kConvThreads == 256 && kEpiThreads == 256, "warp roles");
 };
 
@@ -169,6 +175,8 @@ constexpr int kDBufMax = 16;   // D buffers
 
 struct KParams {
   unsigned long long* amax_keys;   // greedy-argmax variant, else nullptr
+  int s_rps;                       // W8A16: scale rows per 128-wide group (4, 1; 0 = one row)
+  uint32_t s_tx;                   // bytes of one scale-chunk load
   const float* s_a;
   void* out;
   int64_t M, N, G, F, W;
@@ -373,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_s, const KParams p) {
   using C = Cfg<kMode, T>;
   constexpr int NB = C::kNumBuf;
-  constexpr int ND = C::kW4 ? C::kSegBufs : C::kNumD;
+  constexpr int ND = C::kWO ? C::kSegBufs : C::kNumD;
   constexpr int SR = C::kScaleSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -417,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->a_empty[i]), 1);
     }
     for (int i = 0; i < ND; ++i) {
-      mbar_init(smem_u32(&ctrl->d_full[i]), C::kW4 ? C::kIssuers : 1);
+      mbar_init(smem_u32(&ctrl->d_full[i]), C::kWO ? C::kIssuers : 1);
       mbar_init(smem_u32(&ctrl->d_empty[i]), C::kEpiWarps);
     }
     for (int i = 0; i < SR; ++i) {
@@ -506,10 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sph = static_cast<uint32_t>(ch.ci / SR) & 1u;
             if (!mbar_wait(smem_u32(&ctrl->s_empty[slot]), sph ^ 1u, ctx, 11)) break;
             const uint32_t sfull = smem_u32(&ctrl->s_full[slot]);
-            mbar_arrive_expect_tx(sfull, C::kScaleSlotBytes);
+            mbar_arrive_expect_tx(sfull, p.s_tx);
+            const int32_t srow = kMode == kModeW8A16 ? static_cast<int32_t>(it.g * p.s_rps)
+                                                     : static_cast<int32_t>(it.g);
             tma_load_2d(sbase + sc_off + static_cast<uint32_t>(slot) * C::kScaleSlotBytes, &tm_s,
-                        sfull, static_cast<int32_t>(it.f * kTileF), static_cast<int32_t>(it.g),
-                        pol_w);
+                        sfull, static_cast<int32_t>(it.f * kTileF), srow, pol_w);
             ++s_issued;
           }
         }
@@ -553,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warp 1 takes the even steps, warp 3 the odd ones
     if (lane == 0) {
       const int me = warp == 1 ? 0 : 1;
-      constexpr uint32_t idesc = idesc_f16(kTileF, T, C::kW4);
+      constexpr uint32_t idesc = idesc_f16(kTileF, T, C::kWO);
       StepIter it(s0, G, F);
       Ring rx(NX);
       int seg = 0;
@@ -564,13 +573,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ab = j % NB;
         const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
         if (seg_first) started = false;
-        const int didx = C::kW4 ? seg : j;
+        const int didx = C::kWO ? seg : j;
         const int db = didx % ND;
         const uint32_t dbph = static_cast<uint32_t>(didx / ND) & 1u;
-        const uint32_t dcol = C::kW4 ? tmem + C::kColD + (db * C::kIssuers + me) * T
+        const uint32_t dcol = C::kWO ? tmem + C::kColD + (db * C::kIssuers + me) * T
                                      : tmem + C::kColD + db * T;
         if ((j & 1) == me) {
-          const bool need_d = C::kW4 ? !started : true;
+          const bool need_d = C::kWO ? !started : true;
           // in-kernel expansion: a_full also covers the fp16 operand slot
           // (slot ab, written by the same converter group); else the TMA tile
           if (!C::kXConv && !mbar_wait(smem_u32(&ctrl->xfull[rx.slot]), rx.phase, ctx, 3)) break;
@@ -586,17 +595,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the second 64-wide half of the group starts T*128 B further.
             const uint32_t off = static_cast<uint32_t>(ks >> 2) * (T * 128u) +
                                  static_cast<uint32_t>(ks & 3) * 32u;
-            const bool acc = C::kW4 ? (started || ks > 0) : ks > 0;
+            const bool acc = C::kWO ? (started || ks > 0) : ks > 0;
             mma_ts(dcol, tmem + C::kColA + ab * 64 + ks * 8, d0 + (off >> 4), idesc,
                    acc ? 1u : 0u);
           }
-          if constexpr (C::kW4) tc_commit(smem_u32(&ctrl->a_empty[ab]));
+          if constexpr (C::kWO) tc_commit(smem_u32(&ctrl->a_empty[ab]));
           if constexpr (!C::kXConv) tc_commit(smem_u32(&ctrl->xempty[rx.slot]));
           // W8A8: also frees the A buffer (and the fp16 slot of in-kernel expansion)
-          if constexpr (!C::kW4) tc_commit(smem_u32(&ctrl->d_full[db]));
+          if constexpr (!C::kWO) tc_commit(smem_u32(&ctrl->d_full[db]));
           started = true;
         }
-        if constexpr (C::kW4) {
+        if constexpr (C::kWO) {
           if (seg_last) {
             // Every issuer reports on every segment.  One that accumulated
             // nothing into it arrives directly, but only once the epilogue has
@@ -631,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool chunk_ready = false;   // W4A16: this group has waited for the chunk's scales
     for (int j = 0; j < n_steps; ++j, it.next(), rg.next(), ri.next(), ch.advance()) {
       const bool seg_last = (j == n_steps - 1) || (it.g == G - 1);
-      if constexpr (C::kW4) {
+      if constexpr (C::kWO) {
         if (ch.begin(j == 0 || it.g == 0)) chunk_ready = false;
       }
       const bool mine = (j & 1) == grp;
@@ -639,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ab = j % NB;
         const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
         bool ok = mbar_wait(smem_u32(&ctrl->wfull[rg.slot]), rg.phase, ctx, 7);
-        if constexpr (C::kW4) {
+        if constexpr (C::kWO) {
           if (ok) ok = mbar_wait(smem_u32(&ctrl->a_empty[ab]), abph ^ 1u, ctx, 8);
         } else if (ok && j >= NB) {
           // A buffer ab was last read by step j - NB, committed on its D
@@ -652,15 +661,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (C::kXConv && ok) ok = mbar_wait(smem_u32(&ctrl->xfull[ri.slot]), ri.phase, ctx, 3);
         uint32_t s2 = 0;
-        if constexpr (C::kW4) {
+        float sq[4] = {0.f, 0.f, 0.f, 0.f};   // W8A16 scales of the group's quarters
+        if constexpr (C::kWO) {
           const int slot = ch.ci % SR;
           if (ok && !chunk_ready)
             ok = mbar_wait(smem_u32(&ctrl->s_full[slot]), static_cast<uint32_t>(ch.ci / SR) & 1u,
                            ctx, 13);
           if (!warp_all(ok)) break;
           chunk_ready = true;
-          const uint32_t sb = scale_ring[(slot * kScaleChunk + ch.row()) * 128 + r];
-          s2 = sb | (sb << 16);
+          if constexpr (C::kInt4) {
+            const uint32_t sb = scale_ring[(slot * kScaleChunk + ch.row()) * 128 + r];
+            s2 = sb | (sb << 16);
+          } else {
+            // W8A16: the scale of each 32-wide quarter of the group
+            const uint16_t* srow = scale_ring + (slot * C::kScaleRowsMax + ch.row() * p.s_rps) * 128 + r;
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+              sq[h] = __uint_as_float(static_cast<uint32_t>(srow[(p.s_rps == 4 ? h : 0) * 128]) << 16);
+          }
         } else {
           if (!warp_all(ok)) break;
         }
@@ -694,10 +712,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           uint32_t v[16];
-          if constexpr (C::kW4) {
+          if constexpr (C::kInt4) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               int4x8_to_bf16x8(wsm[(h * 4 + i) * kTileF + r], s2, v + 4 * i);
+          } else if constexpr (kMode == kModeW8A16) {
+            // byte u = q + 128 -> exact q in fp32 (2^23 + u minus 2^23 + 128),
+            // q * s exact in fp32, one rounding to bf16
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t w = wsm[(h * 8 + i) * kTileF + r];
+              float f[4];
+#pragma unroll
+              for (int b = 0; b < 4; ++b)
+                f[b] = (__uint_as_float(prmt(w, 0x4B000000u, static_cast<uint32_t>(b | 0x7440))) -
+                        8388736.0f) * sq[h];
+              v[2 * i] = bf16x2_rn(f[0], f[1]);
+              v[2 * i + 1] = bf16x2_rn(f[2], f[3]);
+            }
           } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -714,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(smem_u32(&ctrl->a_full[ab]));
         }
       }
-      if constexpr (C::kW4) {
+      if constexpr (C::kWO) {
         // both groups release each scale chunk (a group that had no step in it
         // read nothing from it)
         if (ch.ends(seg_last)) {
@@ -762,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t m = tt * T + colbase + c;
           uint32_t key = 0u;
           if (nn < N && m < M) {
-            const float v = C::kW4 ? vals[c] : vals[c] * __ldg(p.s_a + m);
+            const float v = C::kWO ? vals[c] : vals[c] * __ldg(p.s_a + m);
             uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
             if (b == 0x8000u) b = 0u;   // -0 equals +0
             const uint32_t ord = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
@@ -784,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < C::kEpiCols; ++c) {
         const int64_t m = tt * T + colbase + c;
         if (m < M) {
-          const float v = C::kW4 ? vals[c] : vals[c] * __ldg(p.s_a + m);
+          const float v = C::kWO ? vals[c] : vals[c] * __ldg(p.s_a + m);
           y[m * N + nn] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
         }
       }
@@ -802,9 +834,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::kEpiCols; ++c) acc[c] = 0.0f;
       }
-      if (!C::kW4 || seg_last) {
+      if (!C::kWO || seg_last) {
         // drain one accumulator buffer: per group (W8A8) or per segment (W4A16)
-        const int idx = C::kW4 ? seg : j;
+        const int idx = C::kWO ? seg : j;
         const int b = idx % ND;
         const uint32_t bph = static_cast<uint32_t>(idx / ND) & 1u;
         float sw = 0.0f;
@@ -826,14 +858,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (alive) {
           tc_fence_after();
           const uint32_t dcol = tmem + lane_off + C::kColD + colbase +
-                                (C::kW4 ? b * C::kIssuers * T : b * T);
+                                (C::kWO ? b * C::kIssuers * T : b * T);
 #pragma unroll
           for (int c0 = 0; c0 < C::kEpiCols; c0 += kCh) {
             uint32_t v[kCh];
             if constexpr (kCh == 16) tmem_ld16(dcol + c0, v);
             else tmem_ld8(dcol + c0, v);
             tmem_wait_ld();
-            if constexpr (C::kW4) {
+            if constexpr (C::kWO) {
               // the issuers' accumulators, summed in issuer order; an issuer
               // that took no step of this segment left its accumulator unused
               const bool both = j > seg_j0;
@@ -873,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(smem_u32(&ctrl->d_empty[b]));
         }
       }
-      if (C::kW4 && seg_last) ++seg;
+      if (C::kWO && seg_last) ++seg;
       if (kMode == kModeP || !seg_last) continue;
 
       // ---- end of this block's segment of the tile (all epilogue warps agree)
@@ -1026,7 +1058,7 @@ template <int kMode, int T>
 cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream_t stream) {
   using C = Cfg<kMode, T>;
   const void* act16 = a.act;
-  if constexpr (!C::kW4 && !C::kXConv) {
+  if constexpr (!C::kWO && !C::kXConv) {
     // int8 activations -> fp16 image in the workspace
     uint16_t* dst = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.workspace) + pl.act_offset);
     const int64_t n16 = a.M * a.K / 16;
@@ -1038,13 +1070,13 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
     act16 = dst;
   }
   CUtensorMap tw, ta;
-  const uint64_t words_rows = static_cast<uint64_t>(a.K) / (C::kW4 ? 8 : 4);
+  const uint64_t words_rows = static_cast<uint64_t>(a.K) / (C::kInt4 ? 8 : 4);
   if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, a.qweight, a.N, words_rows,
                    static_cast<uint64_t>(a.N) * 4, kTileF, C::kWordRows,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   if constexpr (!C::kXConv) {
-    if (!make_act_map(&ta, C::kW4 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+    if (!make_act_map(&ta, C::kWO ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                       act16, a.M, a.K, T))
       return cudaErrorInvalidValue;
   } else {
@@ -1054,9 +1086,15 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
       return cudaErrorInvalidValue;
   }
   CUtensorMap ts;
+  // scale rows per 128-wide group and per chunk load: W8A16 group-32 has 4,
+  // group-128 one, per-column scales one row for all K
+  const int s_rps = kMode != kModeW8A16 ? 1 : (a.group_size == 32 ? 4 : a.group_size == 128 ? 1 : 0);
+  const uint32_t s_box = s_rps == 0 ? 1u : static_cast<uint32_t>(kScaleChunk * s_rps);
+  const uint64_t s_rows = kMode != kModeW8A16 ? static_cast<uint64_t>(a.K / kGroup)
+                          : (a.group_size == 0 ? 1u : static_cast<uint64_t>(a.K / a.group_size));
   if constexpr (C::kScales) {
-    if (!make_map_2d(&ts, C::kW4 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                     a.scales, a.N, a.K / kGroup, static_cast<uint64_t>(a.N) * 2, kTileF, kScaleChunk,
+    if (!make_map_2d(&ts, C::kWO ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     a.scales, a.N, s_rows, static_cast<uint64_t>(a.N) * 2, kTileF, s_box,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   } else {
@@ -1080,6 +1118,8 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
 
   KParams kp;
   kp.amax_keys = a.amax_keys;
+  kp.s_rps = s_rps;
+  kp.s_tx = s_box * 256u;
   kp.s_a = a.s_a;
   kp.out = a.out;
   kp.M = a.M;
@@ -1148,6 +1188,7 @@ cudaError_t launch_gemm(const GemmArgs& a, const GemmPlan& p, int* err, cudaStre
   switch (a.mode) {
     case GemmMode::kW8A8: return launch_mode<kModeW8A8>(a, p, err, stream);
     case GemmMode::kW8A8Partials: return launch_mode<kModeP>(a, p, err, stream);
+    case GemmMode::kW8A16: return launch_mode<kModeW8A16>(a, p, err, stream);
     default: return launch_mode<kModeW4>(a, p, err, stream);
   }
 }

@@ -79,7 +79,8 @@ qlin_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLI
 
 qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const int32_t* qweight,
                        const uint16_t* scales, void* out, int64_t M, int64_t N, int64_t K,
-                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                       int group_size = 128) {
   if (act == nullptr || qweight == nullptr || out == nullptr ||
       (mode != GemmMode::kW8A8Partials && scales == nullptr) ||
       (mode == GemmMode::kW8A8 && s_a == nullptr))
@@ -97,6 +98,7 @@ qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const i
   const GemmPlan plan = plan_gemm(M, N, K, d->sm_count);
   if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return QLIN_ERR_WORKSPACE;
   GemmArgs a{mode, act, s_a, qweight, scales, out, M, N, K, workspace, workspace_bytes};
+  a.group_size = group_size;
   return from_cuda(launch_gemm(a, plan, d->err_word, stream));
 }
 
@@ -164,6 +166,14 @@ qlin_status_t qlin_gemm_w4a16_g128(const uint16_t* x, const int32_t* qweight,
                                    qlin_stream_t stream) {
   return run_gemm(GemmMode::kW4A16, x, nullptr, qweight, scales, y, M, N, K, workspace,
                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_gemm_w8a16(const uint16_t* x, const int32_t* qweight, const uint16_t* scales,
+                              int64_t M, int64_t N, int64_t K, int group_size, uint16_t* y,
+                              void* workspace, size_t workspace_bytes, qlin_stream_t stream) {
+  if (group_size != 0 && group_size != 32 && group_size != 128) return QLIN_ERR_SHAPE;
+  return run_gemm(GemmMode::kW8A16, x, nullptr, qweight, scales, y, M, N, K, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream), group_size);
 }
 
 qlin_status_t qlin_gemm_w8a8_gs128_argmax(const int8_t* q_a, const float* s_a,

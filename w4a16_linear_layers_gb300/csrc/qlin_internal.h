@@ -32,7 +32,7 @@ cudaError_t launch_ingest_nk(const int32_t* packed_nk, const uint16_t* scales_ng
                              cudaStream_t stream);
 
 // GEMM problem description passed from the API to the launcher.
-enum class GemmMode : int { kW8A8 = 0, kW8A8Partials = 1, kW4A16 = 2 };
+enum class GemmMode : int { kW8A8 = 0, kW8A8Partials = 1, kW4A16 = 2, kW8A16 = 3 };
 
 struct GemmArgs {
   GemmMode mode;
@@ -48,6 +48,8 @@ struct GemmArgs {
   // a 64-bit key (order-preserving bf16 bits << 32 | ~n) with atomicMax; the
   // largest key is the largest value, lowest n on ties.  nullptr = write y.
   unsigned long long* amax_keys = nullptr;
+  // W8A16: K-width of a scale group (32 or 128), or 0 for one scale per column
+  int group_size = 128;
 };
 
 // Offset of the argmax keys (one per row, M <= 128) inside the fixed counter

@@ -35,6 +35,7 @@ EXPORTS = (
     "qlin_gemm_w8a8_gs128",
     "qlin_gemm_w8a8_gs128_noalloc",
     "qlin_gemm_w4a16_g128",
+    "qlin_gemm_w8a16",
     "qlin_gemm_w8a8_gs128_argmax",
     "qlin_gemm_w4a16_g128_argmax",
     "qlin_pack_gptq",
@@ -79,6 +80,7 @@ def load():
             "qlin_gemm_w8a8_gs128": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_gemm_w8a8_gs128_noalloc": ([P, P, P, P, I64, I64, I64, P, P], I),
             "qlin_gemm_w4a16_g128": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_gemm_w8a16": ([P, P, P, I64, I64, I64, I, P, P, SZ, P], I),
             "qlin_gemm_w8a8_gs128_argmax": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_gemm_w4a16_g128_argmax": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_pack_gptq": ([P, I64, I64, I, P, P, P], I),
@@ -244,6 +246,27 @@ def gemm_w4a16_g128(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor
     ws = _workspace(workspace, M, N, K, x.device)
     _check(load().qlin_gemm_w4a16_g128(_ptr(x), _ptr(qweight), _ptr(scales), M, N, K, _ptr(y),
                                        _ptr(ws), ws.numel(), _stream_handle(stream)))
+    return y
+
+
+def gemm_w8a16(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, group_size: int,
+               y: torch.Tensor | None = None, workspace=None, stream=None) -> torch.Tensor:
+    """x bf16 [M,K], qweight int32 [K/4,N] (8-bit GPTQ words), scales bf16
+    [K/group_size,N] ([1,N] for group_size 0) -> y bf16 [M,N]."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(qweight, "qweight", torch.int32, 2)
+    _need(scales, "scales", torch.bfloat16, 2)
+    M, K = x.shape
+    N = qweight.shape[1]
+    rows = 1 if group_size == 0 else K // group_size
+    if qweight.shape[0] * 4 != K or scales.shape != (rows, N):
+        raise ValueError("inconsistent W8A16 shapes")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", torch.bfloat16, 2)
+    ws = _workspace(workspace, M, N, K, x.device)
+    _check(load().qlin_gemm_w8a16(_ptr(x), _ptr(qweight), _ptr(scales), M, N, K, int(group_size),
+                                  _ptr(y), _ptr(ws), ws.numel(), _stream_handle(stream)))
     return y
 
 
