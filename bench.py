@@ -57,6 +57,10 @@ def workload_specs(name: str):
         for M in (8, 64):
             for lname, K, N, kind in synth.drafter_linears():
                 specs.append((lname, K, N, "normal", M, "w4a16"))
+    elif name == "w8a16":
+        for M in (8, 64):
+            for lname, K, N, kind in synth.DRAFTER_LAYER:
+                specs.append((f"layers.0.{lname}", K, N, "normal", M, "w8a16"))
     elif name == "prefill":
         for M in (128, 512, 2048, 8192):
             specs.append(("layers.0.gate_proj", 5120, 17408, "outliers", M, "w8a8"))
@@ -78,14 +82,20 @@ WORKLOAD_DESC = {
     "single": "single W8A8 GS128 linear 5120->1024, M=8",
     "drafter": "full drafter: 35 W8A8 GS128 linears + fc 25600->5120, M=96",
     "w4a16": "full drafter in W4A16 g128 (36 linears), M in {8,64}",
+    "w8a16": "drafter layer: 7 W8A16 group-32 linears x M in {8,64}",
     "prefill": "W8A8 GS128 gate/up 5120->17408 + down 17408->5120, M in {128,512,2048,8192}",
     "vocab": "W8A8 GS128 vocab head 5120->248320, M in {8,96}",
     "vocab_argmax": "W8A8 GS128 vocab head 5120->248320 with fused greedy argmax, M in {8,96}",
 }
 
 
+W8A16_GROUP = 32   # the bench's W8A16 scale group (the DFlash2 recipe's group-32 int8)
+
+
 def weight_bytes(K, N, kind):
     kind = kind.replace("_argmax", "")
+    if kind == "w8a16":
+        return K * N + 2 * (K // W8A16_GROUP) * N
     return (K * N if kind == "w8a8" else K * N // 2) + 2 * (K // 128) * N
 
 
@@ -96,7 +106,7 @@ def gemm_algo_bytes(M, K, N, kind):
     greedy-argmax variant)."""
     out = 4 * M if kind.endswith("_argmax") else 2 * M * N
     kind = kind.replace("_argmax", "")
-    act = M * K * (1 if kind == "w8a8" else 2) + (4 * M if kind == "w8a8" else 0)
+    act = M * K * (1 if kind == "w8a8" else 2) + (4 * M if kind == "w8a8" else 0)   # w4a16/w8a16: bf16 x
     return weight_bytes(K, N, kind) + act + out
 
 
@@ -228,6 +238,11 @@ class LayerRunner:
                     qd = torch.from_numpy(q).to(device)
                     qw, _ = qlin.pack_gptq(qd, 8, with_qzeros=False)
                     sd = torch.from_numpy(s.view(np.int16)).view(torch.float16).to(device)
+                elif wk == "w8a16":
+                    q, s = synth.w8a16_weights(seed, name + "/w8a16", K, N, W8A16_GROUP)
+                    qd = torch.from_numpy(q).to(device)
+                    qw, _ = qlin.pack_gptq(qd, 8, with_qzeros=False)
+                    sd = torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).to(device)
                 else:
                     q, s = synth.w4a16_weights(seed, name + "/w4", K, N)
                     qd = torch.from_numpy(q).to(device)
@@ -307,6 +322,9 @@ class LayerRunner:
             elif c["wk"] == "w8a8":
                 q, s = self.acts[c["ikey"]]
                 self.qlin.gemm_w8a8_gs128(q, s, c["qw"], c["sc"], c["y"], workspace=ws)
+            elif c["wk"] == "w8a16":
+                self.qlin.gemm_w8a16(self.inputs[c["ikey"]], c["qw"], c["sc"], W8A16_GROUP, c["y"],
+                                     workspace=ws)
             else:
                 self.qlin.gemm_w4a16_g128(self.inputs[c["ikey"]], c["qw"], c["sc"], c["y"],
                                           workspace=ws)
@@ -529,6 +547,8 @@ def oracle_sample(specs, budget_s, seed=0, cache=None):
         if key not in cache:
             if wk.startswith("w8a8"):
                 cache[key] = synth.w8a8_weights(seed, name, K, N)
+            elif wk == "w8a16":
+                cache[key] = synth.w8a16_weights(seed, name + "/w8a16", K, N, W8A16_GROUP)
             else:
                 cache[key] = synth.w4a16_weights(seed, name + "/w4", K, N)
         q, s = cache[key]
@@ -538,6 +558,9 @@ def oracle_sample(specs, budget_s, seed=0, cache=None):
             qw, _, _ = oracle.pack_gptq(q, 8)
             qa, sa = oracle.act_quant_i8(xb)
             return (lambda ch, a=(qa, sa, qw, s, K): oracle.gemm_w8a8_gs128(*a, cols=ch))
+        if wk == "w8a16":
+            qw, _, _ = oracle.pack_gptq(q, 8)
+            return (lambda ch, a=(xb, qw, s, K): oracle.gemm_w8a16(*a, W8A16_GROUP, cols=ch))
         qw, _, _ = oracle.pack_gptq(q, 4)
         return (lambda ch, a=(xb, qw, s, K): oracle.gemm_w4a16_g128(*a, cols=ch))
 
