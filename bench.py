@@ -401,9 +401,10 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         step_graph.replay()
     torch.cuda.synchronize()
-    st = qlin.device_status()
+    st, where, block = qlin.device_error_detail()
     if st != qlin.QLIN_OK:
-        raise SystemExit(f"device status after warm-up: {qlin.status_string(st)}")
+        raise SystemExit(f"device status after warm-up: {qlin.status_string(st)} "
+                         f"(wait {where}, block {block})")
 
     clocks = ClockSampler(local_rank)
     if dist:
@@ -447,9 +448,10 @@ def run_ours(args, rank, world, local_rank):
         t = torch.tensor([t_e2e], device=device, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         t_e2e = t.item()
-    st = qlin.device_status()
+    st, where, block = qlin.device_error_detail()
     if st != qlin.QLIN_OK:
-        raise SystemExit(f"device status after timing: {qlin.status_string(st)}")
+        raise SystemExit(f"device status after timing: {qlin.status_string(st)} "
+                         f"(wait {where}, block {block})")
 
     if rank != 0:
         return None

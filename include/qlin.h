@@ -303,6 +303,15 @@ qlin_status_t qlin_debug_wait_timeout(int64_t limit_ns, qlin_stream_t stream);
  */
 qlin_status_t qlin_device_status(qlin_stream_t stream);
 
+/*
+ * The device error word without clearing it: returns the status
+ * qlin_device_status would return and, when it is not QLIN_OK, the code
+ * location of the failing wait or check (`where`, a small integer naming the
+ * role and the wait inside the kernel) and the index of the thread block that
+ * recorded it.  Synchronizes `stream`.  Either output may be NULL.
+ */
+qlin_status_t qlin_device_error_detail(qlin_stream_t stream, int32_t *where, int32_t *block);
+
 /* A static, human-readable name for a status code. */
 const char *qlin_status_string(qlin_status_t status);
 

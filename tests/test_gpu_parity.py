@@ -144,6 +144,7 @@ def _gemm_w8a8_gpu(qa, sa, qw, swb, workspace=None):
 @pytest.mark.parametrize("M,K,N", [
     (1, 128, 128), (3, 256, 200), (8, 5120, 1024), (16, 1280, 384), (17, 640, 256),
     (64, 4096, 512), (96, 2560, 768), (100, 384, 136), (128, 512, 256), (257, 768, 264),
+    (8, 128, 2048),   # one group: every step opens its own scale chunk
 ])
 def test_w8a8_matches_oracle(M, K, N):
     _, qa, sa, _, qw, swb = _w8a8_inputs(5, f"gpu/w8/{M}/{K}/{N}", M, K, N)
@@ -209,6 +210,8 @@ def _gemm_w4a16_gpu(xb, qw, sb, workspace=None):
 @pytest.mark.parametrize("M,K,N", [
     (1, 128, 128), (3, 256, 200), (8, 5120, 1024), (17, 640, 256), (64, 4096, 512),
     (96, 1280, 384), (130, 512, 264),
+    # one (two-group) step per tile: every step opens its own scale chunk
+    (8, 128, 2048), (8, 256, 2048), (64, 256, 4096),
 ])
 def test_w4a16_matches_oracle(M, K, N):
     xb, _, qw, sb = _w4a16_inputs(9, f"gpu/w4/{M}/{K}/{N}", M, K, N)
@@ -405,7 +408,7 @@ def _w8a16_inputs(seed, name, M, K, N, gs):
 
 @pytest.mark.parametrize("gs", [32, 128, 0])
 @pytest.mark.parametrize("M,K,N", [(1, 128, 128), (8, 5120, 1024), (17, 640, 264), (64, 1280, 384),
-                                   (96, 384, 136), (130, 256, 200)])
+                                   (96, 384, 136), (130, 256, 200), (8, 128, 2048)])
 def test_w8a16_matches_oracle(M, K, N, gs):
     xb, qw, sb = _w8a16_inputs(16, f"gpu/w8a16/{M}/{K}/{N}/{gs}", M, K, N, gs)
     y = qlin.gemm_w8a16(to_dev_bits(xb, torch.bfloat16), to_dev(qw), to_dev_bits(sb, torch.bfloat16), gs)
@@ -432,3 +435,40 @@ def test_w8a16_rejects_other_group_sizes():
     with pytest.raises(qlin.QlinError) as e:
         qlin.gemm_w8a16(x, qw, sc, 64)
     assert e.value.status == qlin.QLIN_ERR_SHAPE
+
+
+# ------------------------------------------------- repeated back-to-back launches
+
+@pytest.mark.parametrize("fmt,M,K,N", [("w4a16", 8, 5120, 17408), ("w4a16", 8, 4096, 5120),
+                                       ("w4a16", 64, 17408, 5120), ("w8a8", 8, 5120, 17408),
+                                       ("w8a8", 96, 5120, 6144), ("w8a16", 8, 5120, 6144)])
+def test_repeated_launches_are_identical(fmt, M, K, N):
+    """Hundreds of launches of one full-size linear, back to back on one
+    stream with one workspace: no bounded wait may run out, and every launch
+    must reproduce the first one's output bit for bit (the split-tile fix-up
+    sums in a fixed order)."""
+    reps = 300
+    if fmt == "w8a8":
+        _, qa, sa, _, qw, swb = _w8a8_inputs(20, f"gpu/rep/{M}/{K}/{N}", M, K, N)
+        args = (to_dev(qa), to_dev(sa), to_dev(qw), to_dev_bits(swb, torch.float16))
+        fn = qlin.gemm_w8a8_gs128
+    elif fmt == "w4a16":
+        xb, _, qw, sb = _w4a16_inputs(20, f"gpu/rep4/{M}/{K}/{N}", M, K, N)
+        args = (to_dev_bits(xb, torch.bfloat16), to_dev(qw), to_dev_bits(sb, torch.bfloat16))
+        fn = qlin.gemm_w4a16_g128
+    else:
+        xb, qw, sb = _w8a16_inputs(20, f"gpu/rep8/{M}/{K}/{N}", M, K, N, 32)
+        args = (to_dev_bits(xb, torch.bfloat16), to_dev(qw), to_dev_bits(sb, torch.bfloat16), 32)
+        fn = qlin.gemm_w8a16
+    ws = torch.zeros(qlin.workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    first = fn(*args, workspace=ws)
+    torch.cuda.synchronize()
+    y = torch.empty_like(first)
+    mismatches = torch.zeros((), dtype=torch.int64, device="cuda")
+    for _ in range(reps):
+        fn(*args, y=y, workspace=ws)
+        mismatches += (y.view(torch.int16) != first.view(torch.int16)).sum()
+    st, where, block = qlin.device_error_detail()
+    qlin.device_status()
+    assert st == qlin.QLIN_OK, f"{qlin.status_string(st)} (wait {where}, block {block})"
+    assert int(mismatches) == 0

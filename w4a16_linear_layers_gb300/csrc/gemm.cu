@@ -83,12 +83,19 @@ constexpr int kModeP = 1;     // W8A8 pipeline, exports the group partials
 constexpr int kModeW4 = 2;
 constexpr int kModeW8A16 = 3;   // int8 weight-only: group-32, group-128 or per-column scales
 
-template <int kMode, int T>
+template <int kMode, int T, int GPS = 1>
 struct Cfg {
   // weight-only formats (W4A16, W8A16): bf16 tokens, scales applied by the
   // converters, the whole K accumulated in TMEM
   static constexpr bool kWO = kMode == kModeW4 || kMode == kModeW8A16;
   static constexpr bool kInt4 = kMode == kModeW4;
+  // 128-wide K groups per pipeline step.  W4A16 at token tiles up to 32 takes
+  // two: a step then carries 16 KB of weights like the 8-bit formats, which
+  // halves the fixed per-step cost (synchronisation, MMA issue) per byte.  At
+  // 64-token tiles the larger activation slots would halve the weight bytes
+  // in flight, and two-group steps measured no faster there.
+  static constexpr int kGPS = GPS;
+  static_assert(GPS == 1 || (GPS == 2 && kInt4 && T <= 32), "two-group steps: W4A16, T <= 32");
   // warps 0..3: control (0 weight TMA, 1 TMEM owner + MMA issuer, 2 activation
   //             and scale TMA, 3 MMA issuer)
   // warps 4..11: converters, two groups of four taking alternate steps (each
@@ -102,9 +109,10 @@ struct Cfg {
   static constexpr int kEpiWarps = 8;
   static constexpr int kConvThreads = 32 * kConvWarps;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
-  static constexpr int kWordRows = kInt4 ? 16 : 32;         // int32 rows per group
+  static constexpr int kWordRows = (kInt4 ? 16 : 32) * GPS;  // int32 rows per step
   static constexpr uint32_t kWBytes = kWordRows * kTileF * 4;
-  static constexpr uint32_t kABytes = 2u * T * 128u;         // two 64-wide 16-bit halves
+  static constexpr uint32_t kABytes = 2u * T * 128u * GPS;   // 64-wide 16-bit halves
+  static constexpr int kACols = 64 * GPS;                     // TMEM columns per A buffer
   // Weights and activations travel in rings of their own, so neither stream
   // waits for the other's consumer.  A weight slot is freed as soon as the
   // converters have moved it into TMEM.
@@ -135,8 +143,11 @@ struct Cfg {
   // W8A8 sizes the A buffers (converter -> MMA) and the D buffers (MMA ->
   // epilogue) separately: the epilogue loop (MMA completion, TMEM drain,
   // release) is the long one, so small token tiles get many D buffers.
-  static constexpr int kNumBufRaw = kWO ? (512 - kW4DCols) / 64 : (T <= 64 ? 4 : 2);
-  static constexpr int kNumBuf = kNumBufRaw < 6 ? kNumBufRaw : 6;
+  static constexpr int kNumBufRaw = kWO ? (512 - kW4DCols) / kACols : (T <= 64 ? 4 : 2);
+  // An even count keeps every A buffer with one converter group and one
+  // issuer (steps alternate between the two of each).
+  static constexpr int kNumBufCap = kNumBufRaw < 6 ? kNumBufRaw : 6;
+  static constexpr int kNumBuf = kNumBufCap - (kNumBufCap & 1);
   static constexpr int kNumDFit = kWO ? 1 : (512 - 64 * kNumBuf) / T;
   static constexpr int kNumDRaw = kNumDFit < 16 ? kNumDFit : 16;
   // ND - NA even: see the waits of the converters
@@ -149,7 +160,7 @@ struct Cfg {
                 "one commit per step needs ND >= NA with ND - NA even");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColA = 0;
-  static constexpr uint32_t kColD = 64 * kNumBuf;
+  static constexpr uint32_t kColD = kACols * kNumBuf;
   static constexpr int kEpiCols = T / 2;                     // columns per epilogue thread
   // a weight slot is released by the four warps of one converter group
   static constexpr uint32_t kEmptyCount = kConvWarps / 2;
@@ -159,7 +170,7 @@ struct Cfg {
   static constexpr bool kScales = kMode != kModeP;
   static constexpr int kScaleSlots = 4;
   // W8A16 group-32 scales bring 4 rows per 128-wide group
-  static constexpr uint32_t kScaleRowsMax = kMode == kModeW8A16 ? 4 * kScaleChunk : kScaleChunk;
+  static constexpr uint32_t kScaleRowsMax = (kMode == kModeW8A16 ? 4 : GPS) * kScaleChunk;
   static constexpr uint32_t kScaleSlotBytes = kScaleRowsMax * 256u;
   static constexpr uint32_t kScaleBytes = kScales ? kScaleSlots * kScaleSlotBytes : 0u;
   static_assert(T % 16 == 0 && T >= 16 && T <= 128, "token tile");
@@ -374,12 +385,12 @@ __device__ __forceinline__ bool split_finish(const KParams& p, Ctrl* ctrl, const
   return true;
 }
 
-template <int kMode, int T>
+template <int kMode, int T, int GPS>
 __global__ void __launch_bounds__(kThreads, 1)
     qlin_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                      const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_s, const KParams p) {
-  using C = Cfg<kMode, T>;
+  using C = Cfg<kMode, T, GPS>;
   constexpr int NB = C::kNumBuf;
   constexpr int ND = C::kWO ? C::kSegBufs : C::kNumD;
   constexpr int SR = C::kScaleSlots;
@@ -512,11 +523,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ch.begin(j == 0 || it.g == 0)) {
             const int slot = ch.ci % SR;
             const uint32_t sph = static_cast<uint32_t>(ch.ci / SR) & 1u;
+            // Short segments can fill the scale ring before the first
+            // activation tiles are all issued; the ring drains only as the
+            // weights flow, so release the weight producer before waiting.
+            if (!go && ch.ci >= SR) {
+              mbar_arrive(smem_u32(&ctrl->x_go));
+              go = true;
+            }
             if (!mbar_wait(smem_u32(&ctrl->s_empty[slot]), sph ^ 1u, ctx, 11)) break;
             const uint32_t sfull = smem_u32(&ctrl->s_full[slot]);
             mbar_arrive_expect_tx(sfull, p.s_tx);
             const int32_t srow = kMode == kModeW8A16 ? static_cast<int32_t>(it.g * p.s_rps)
-                                                     : static_cast<int32_t>(it.g);
+                                                     : static_cast<int32_t>(it.g * GPS);
             tma_load_2d(sbase + sc_off + static_cast<uint32_t>(slot) * C::kScaleSlotBytes, &tm_s,
                         sfull, static_cast<int32_t>(it.f * kTileF), srow, pol_w);
             ++s_issued;
@@ -534,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // one load brings both 64-wide halves of the group, each as a T x
           // 128 B swizzled tile (the activations seen as [K/64][M][64])
           tma_load_3d(dst, &tm_a, full, 0, static_cast<int32_t>(it.t * T),
-                      static_cast<int32_t>(it.g * 2), pol_a);
+                      static_cast<int32_t>(it.g * 2 * GPS), pol_a);
         } else {
           // the group's int8 tile, T rows x 128 B, 128-byte swizzled
           const uint32_t dst = sbase + xi_off + static_cast<uint32_t>(rg.slot) * C::kXiBytes;
@@ -543,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       static_cast<int32_t>(it.t * T), pol_a);
         }
         ++issued;
-        if (issued == x_first) {
+        if (!go && issued == x_first) {
           mbar_arrive(smem_u32(&ctrl->x_go));
           go = true;
         }
@@ -589,14 +607,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t xb = sbase + x_off + static_cast<uint32_t>(rx.slot) * C::kABytes;
           const uint64_t d0 = smem_desc(xb, 16u, 1024u, 2u);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
+          for (int ks = 0; ks < 8 * GPS; ++ks) {
             // 128-byte swizzled K-major 16-bit tile: 8-row groups 1024 B
             // apart, K advanced by 32 B (16 elements) inside the 128-byte row;
             // the second 64-wide half of the group starts T*128 B further.
             const uint32_t off = static_cast<uint32_t>(ks >> 2) * (T * 128u) +
                                  static_cast<uint32_t>(ks & 3) * 32u;
             const bool acc = C::kWO ? (started || ks > 0) : ks > 0;
-            mma_ts(dcol, tmem + C::kColA + ab * 64 + ks * 8, d0 + (off >> 4), idesc,
+            mma_ts(dcol, tmem + C::kColA + ab * C::kACols + ks * 8, d0 + (off >> 4), idesc,
                    acc ? 1u : 0u);
           }
           if constexpr (C::kWO) tc_commit(smem_u32(&ctrl->a_empty[ab]));
@@ -660,7 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                          ctx, 8);
         }
         if (C::kXConv && ok) ok = mbar_wait(smem_u32(&ctrl->xfull[ri.slot]), ri.phase, ctx, 3);
-        uint32_t s2 = 0;
+        uint32_t s2g[GPS];                     // W4A16: bf16x2 scale of each group of the step
+#pragma unroll
+        for (int gi = 0; gi < GPS; ++gi) s2g[gi] = 0u;
         float sq[4] = {0.f, 0.f, 0.f, 0.f};   // W8A16 scales of the group's quarters
         if constexpr (C::kWO) {
           const int slot = ch.ci % SR;
@@ -670,8 +690,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!warp_all(ok)) break;
           chunk_ready = true;
           if constexpr (C::kInt4) {
-            const uint32_t sb = scale_ring[(slot * kScaleChunk + ch.row()) * 128 + r];
-            s2 = sb | (sb << 16);
+#pragma unroll
+            for (int gi = 0; gi < GPS; ++gi) {
+              const uint32_t sb = scale_ring[(slot * C::kScaleRowsMax + ch.row() * GPS + gi) * 128 + r];
+              s2g[gi] = sb | (sb << 16);
+            }
           } else {
             // W8A16: the scale of each 32-wide quarter of the group
             const uint16_t* srow = scale_ring + (slot * C::kScaleRowsMax + ch.row() * p.s_rps) * 128 + r;
@@ -708,14 +731,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t* wsm = reinterpret_cast<const uint32_t*>(
             smem + static_cast<uint32_t>(rg.slot) * C::kStageBytes);
-        const uint32_t acol = tmem + lane_off + C::kColA + ab * 64;
+        const uint32_t acol = tmem + lane_off + C::kColA + ab * C::kACols;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+        for (int h = 0; h < 4 * GPS; ++h) {
           uint32_t v[16];
           if constexpr (C::kInt4) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              int4x8_to_bf16x8(wsm[(h * 4 + i) * kTileF + r], s2, v + 4 * i);
+              int4x8_to_bf16x8(wsm[(h * 4 + i) * kTileF + r], s2g[h >> 2], v + 4 * i);
           } else if constexpr (kMode == kModeW8A16) {
             // byte u = q + 128 -> exact q in fp32 (2^23 + u minus 2^23 + 128),
             // q * s exact in fp32, one rounding to bf16
@@ -1022,14 +1045,14 @@ EncodeFn encode_fn() {
 
 // 16-bit activations [M][K] seen as a 3D tensor {64 (k inside a half group),
 // M (rows, stride K*2 bytes), K/64 (half groups, stride 128 bytes)}; a box
-// {64, T, 2} is one 128-wide K group as two swizzled T x 128 B tiles.
+// {64, T, 2g} is g 128-wide K groups as 2g swizzled T x 128 B tiles.
 bool make_act_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t M,
-                  uint64_t K, uint32_t T) {
+                  uint64_t K, uint32_t T, uint32_t halves) {
   EncodeFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {64, M, K / 64};
   const cuuint64_t strides[2] = {K * 2, 128};
-  const cuuint32_t box[3] = {64, T, 2};
+  const cuuint32_t box[3] = {64, T, halves};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1054,9 +1077,19 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, 
 
 namespace {
 
-template <int kMode, int T>
-cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream_t stream) {
-  using C = Cfg<kMode, T>;
+template <int kMode, int T, int GPS>
+cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl_in, int* err, cudaStream_t stream) {
+  using C = Cfg<kMode, T, GPS>;
+  // steps of GPS groups: fewer (tile, step) units, never more blocks; the
+  // minimum work per block stays kMinSteps groups
+  GemmPlan pl = pl_in;
+  if (GPS > 1) {
+    pl.G = pl_in.G / GPS;
+    pl.steps = pl.TT * pl.F * pl.G;
+    const int64_t by_work = (pl.steps * GPS + kMinSteps - 1) / kMinSteps;
+    pl.ctas = by_work < pl_in.ctas ? by_work : pl_in.ctas;
+    if (pl.ctas < 1) pl.ctas = 1;
+  }
   const void* act16 = a.act;
   if constexpr (!C::kWO && !C::kXConv) {
     // int8 activations -> fp16 image in the workspace
@@ -1077,7 +1110,7 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
     return cudaErrorInvalidValue;
   if constexpr (!C::kXConv) {
     if (!make_act_map(&ta, C::kWO ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                      act16, a.M, a.K, T))
+                      act16, a.M, a.K, T, 2 * GPS))
       return cudaErrorInvalidValue;
   } else {
     // int8 q_a [M][K]: one box is a 128-wide group of T rows, 128-byte swizzled
@@ -1089,7 +1122,8 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
   // scale rows per 128-wide group and per chunk load: W8A16 group-32 has 4,
   // group-128 one, per-column scales one row for all K
   const int s_rps = kMode != kModeW8A16 ? 1 : (a.group_size == 32 ? 4 : a.group_size == 128 ? 1 : 0);
-  const uint32_t s_box = s_rps == 0 ? 1u : static_cast<uint32_t>(kScaleChunk * s_rps);
+  const uint32_t s_box = kMode != kModeW8A16 ? static_cast<uint32_t>(kScaleChunk * GPS)
+                         : (s_rps == 0 ? 1u : static_cast<uint32_t>(kScaleChunk * s_rps));
   const uint64_t s_rows = kMode != kModeW8A16 ? static_cast<uint64_t>(a.K / kGroup)
                           : (a.group_size == 0 ? 1u : static_cast<uint64_t>(a.K / a.group_size));
   if constexpr (C::kScales) {
@@ -1110,7 +1144,7 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(qlin_gemm_kernel<kMode, T>,
+    attr_err = cudaFuncSetAttribute(qlin_gemm_kernel<kMode, T, GPS>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmemLimit));
   });
@@ -1132,18 +1166,22 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream
   kp.err = err;
   kp.limit_ns = kWaitLimitNs;
   kp.stages = stages;
-  return launch_pdl(qlin_gemm_kernel<kMode, T>, dim3(static_cast<unsigned>(pl.ctas)),
+  return launch_pdl(qlin_gemm_kernel<kMode, T, GPS>, dim3(static_cast<unsigned>(pl.ctas)),
                     dim3(kThreads), smem, stream, tw, ta, ts, kp);
 }
 
 template <int kMode>
 cudaError_t launch_mode(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStream_t stream) {
   switch (pl.T) {
-    case 16: return launch_t<kMode, 16>(a, pl, err, stream);
-    case 32: return launch_t<kMode, 32>(a, pl, err, stream);
-    case 64: return launch_t<kMode, 64>(a, pl, err, stream);
-    case 96: return launch_t<kMode, 96>(a, pl, err, stream);
-    default: return launch_t<kMode, 128>(a, pl, err, stream);
+    case 16:
+      if (kMode == kModeW4 && a.K % 256 == 0) return launch_t<kMode, 16, kMode == kModeW4 ? 2 : 1>(a, pl, err, stream);
+      return launch_t<kMode, 16, 1>(a, pl, err, stream);
+    case 32:
+      if (kMode == kModeW4 && a.K % 256 == 0) return launch_t<kMode, 32, kMode == kModeW4 ? 2 : 1>(a, pl, err, stream);
+      return launch_t<kMode, 32, 1>(a, pl, err, stream);
+    case 64: return launch_t<kMode, 64, 1>(a, pl, err, stream);
+    case 96: return launch_t<kMode, 96, 1>(a, pl, err, stream);
+    default: return launch_t<kMode, 128, 1>(a, pl, err, stream);
   }
 }
 

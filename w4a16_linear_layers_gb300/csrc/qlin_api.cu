@@ -267,6 +267,22 @@ qlin_status_t qlin_device_status(qlin_stream_t stream) {
   return QLIN_OK;
 }
 
+qlin_status_t qlin_device_error_detail(qlin_stream_t stream, int32_t* where, int32_t* block) {
+  const DeviceInfo* d = nullptr;
+  qlin_status_t st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return QLIN_ERR_CUDA;
+  int word[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(word, d->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return QLIN_ERR_CUDA;
+  if (where) *where = word[1];
+  if (block) *block = word[2];
+  if (word[0] == kDevTimeout) return QLIN_ERR_DEVICE_TIMEOUT;
+  if (word[0] == kDevValueRange) return QLIN_ERR_VALUE_RANGE;
+  return QLIN_OK;
+}
+
 const char* qlin_status_string(qlin_status_t status) {
   switch (status) {
     case QLIN_OK: return "ok";

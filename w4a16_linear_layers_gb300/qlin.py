@@ -44,6 +44,7 @@ EXPORTS = (
     "qlin_debug_group_partials_i8",
     "qlin_debug_wait_timeout",
     "qlin_device_status",
+    "qlin_device_error_detail",
     "qlin_status_string",
     "qlin_version",
 )
@@ -89,6 +90,7 @@ def load():
             "qlin_debug_group_partials_i8": ([P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_debug_wait_timeout": ([I64, P], I),
             "qlin_device_status": ([P], I),
+            "qlin_device_error_detail": ([P, P, P], I),
             "qlin_status_string": ([I], ctypes.c_char_p),
             "qlin_version": ([], I),
         }
@@ -370,6 +372,14 @@ def debug_group_partials_i8(q_a: torch.Tensor, qweight: torch.Tensor, P: torch.T
 
 def debug_wait_timeout(limit_ns: int, stream=None) -> None:
     _check(load().qlin_debug_wait_timeout(int(limit_ns), _stream_handle(stream)))
+
+
+def device_error_detail(stream=None):
+    """(status, where, block) of the device error word, without clearing it."""
+    w = ctypes.c_int32(0)
+    b = ctypes.c_int32(0)
+    st = int(load().qlin_device_error_detail(_stream_handle(stream), ctypes.byref(w), ctypes.byref(b)))
+    return st, int(w.value), int(b.value)
 
 
 def device_status(stream=None) -> int:
