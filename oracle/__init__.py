@@ -19,6 +19,10 @@ patterns):
 * ``dequant_w4a16(qweight, scales, K, N)`` -> w bf16 bits [K,N]
 * ``argmax_bf16_rows(y_bits)``        -> int32 [M], greedy token per row
 * ``ingest_nk(packed_nk, scales_ng, K, N, bits)`` -> (qweight [K*bits/32,N], scales [K/128,N])
+* ``rmsnorm_bf16(x_bits, gamma_bits, eps)`` -> z bf16 bits [M,K] (decoder RMSNorm)
+* ``silu_mul_bf16(gate_up_bits)``      -> z bf16 bits [M,I] (SiLU(gate) * up)
+* ``rmsnorm_act_quant_i8`` / ``silu_mul_act_quant_i8`` -> (q, s, z): the producer, then act-quant
+* ``f64_to_bf16(v)``                   -> bf16 bits of one binary64 value
 """
 from __future__ import annotations
 
@@ -87,6 +91,12 @@ def _load():
             lib.orc_ingest_nk.restype = None
             lib.orc_gemm_w8a16.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, P, P]
             lib.orc_gemm_w8a16.restype = None
+            lib.orc_f64_to_bf16.argtypes = [ctypes.c_double]
+            lib.orc_f64_to_bf16.restype = ctypes.c_uint16
+            lib.orc_rmsnorm_bf16.argtypes = [P, P, ctypes.c_double, I, I, P]
+            lib.orc_rmsnorm_bf16.restype = None
+            lib.orc_silu_mul_bf16.argtypes = [P, I, I, P]
+            lib.orc_silu_mul_bf16.restype = None
             _lib = lib
     return _lib
 
@@ -259,3 +269,47 @@ def ingest_nk(packed_nk, scales_ng_bits, K: int, N: int, bits: int):
     so = np.empty((K // 128, N), np.uint16)
     _load().orc_ingest_nk(_ptr(pk), _ptr(sc), K, N, bits, _ptr(qw), _ptr(so))
     return qw, so
+
+
+# ------------------------------------------------------------ fused producers
+
+def f64_to_bf16(v: float) -> int:
+    """One binary64 value -> bf16 bits, rounded once (ties to even)."""
+    return int(_load().orc_f64_to_bf16(float(v)))
+
+
+def rmsnorm_bf16(x_bits: np.ndarray, gamma_bits: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of bf16 rows [M, K] with bf16 weight [K] -> bf16 bits [M, K]."""
+    x = _c(x_bits, np.uint16)
+    g = _c(gamma_bits, np.uint16)
+    M, K = x.shape
+    assert g.shape == (K,)
+    z = np.empty((M, K), np.uint16)
+    _load().orc_rmsnorm_bf16(_ptr(x), _ptr(g), float(eps), M, K, _ptr(z))
+    return z
+
+
+def silu_mul_bf16(gate_up_bits: np.ndarray) -> np.ndarray:
+    """bf16 [M, 2I] (gate columns first, then up) -> bf16 bits [M, I]."""
+    gu = _c(gate_up_bits, np.uint16)
+    M, I2 = gu.shape
+    assert I2 % 2 == 0
+    z = np.empty((M, I2 // 2), np.uint16)
+    _load().orc_silu_mul_bf16(_ptr(gu), M, I2 // 2, _ptr(z))
+    return z
+
+
+def rmsnorm_act_quant_i8(x_bits: np.ndarray, gamma_bits: np.ndarray, eps: float):
+    """RMSNorm, then dynamic per-token INT8 quantization of its bf16 output:
+    (q int8 [M,K], s float32 [M], z bf16 bits [M,K])."""
+    z = rmsnorm_bf16(x_bits, gamma_bits, eps)
+    q, s = act_quant_i8(z)
+    return q, s, z
+
+
+def silu_mul_act_quant_i8(gate_up_bits: np.ndarray):
+    """SiLU(gate) * up, then dynamic per-token INT8 quantization of its bf16
+    output: (q int8 [M,I], s float32 [M], z bf16 bits [M,I])."""
+    z = silu_mul_bf16(gate_up_bits)
+    q, s = act_quant_i8(z)
+    return q, s, z

@@ -360,3 +360,72 @@ void orc_gemm_w8a16(const uint16_t *x, const int32_t *qweight, const uint16_t *s
         }
     }
 }
+
+/* ------------------------------------------------------ fused producers */
+
+/* binary64 -> bf16, rounded once to nearest, ties to even.  The value is
+ * scaled so that its bf16 unit in the last place becomes 1 (2^-133 at the
+ * bottom of the subnormal range), rounded to an integer by nearbyint under the
+ * default rounding mode, and scaled back: every step is exact except the one
+ * rounding.  Values that round past the largest finite bf16 give infinity. */
+uint16_t orc_f64_to_bf16(double d)
+{
+    if (isnan(d)) return (uint16_t)0x7fc0u;
+    const int neg = signbit(d) != 0;
+    const double a = fabs(d);
+    if (a == 0.0) return neg ? (uint16_t)0x8000u : (uint16_t)0;
+    int e;
+    (void)frexp(a, &e);                   /* a = f * 2^e, f in [0.5, 1) */
+    int ulp_exp = e - 8;                  /* 8 significant bits */
+    if (ulp_exp < -133) ulp_exp = -133;   /* subnormal bf16 spacing */
+    const double r = ldexp(nearbyint(ldexp(a, -ulp_exp)), ulp_exp);
+    const float f = (float)r;             /* exact, or infinity on overflow */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t h = (uint16_t)(u >> 16);
+    if (neg) h |= (uint16_t)0x8000u;
+    return h;
+}
+
+/* RMSNorm of each bf16 row, as the decoder norms of the model family define
+ * it ("Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card: input_layernorm and
+ * post_attention_layernorm are kept in BF16, in front of the q/k/v and
+ * gate/up projections):
+ *   variance = mean_k x[m,k]^2,   t = bf16(x / sqrt(variance + eps)),
+ *   z[m,k] = bf16(gamma[k] * t).
+ * Evaluated in fp64 and rounded where the definition stores bf16 (the
+ * product of two bf16 values is exact in fp64). */
+void orc_rmsnorm_bf16(const uint16_t *x, const uint16_t *gamma, double eps, int64_t M, int64_t K,
+                      uint16_t *z)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = x + m * K;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double v = (double)orc_bf16_to_f32(row[k]);
+            ss += v * v;
+        }
+        const double rstd = 1.0 / sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k) {
+            const double t = (double)orc_bf16_to_f32(orc_f64_to_bf16((double)orc_bf16_to_f32(row[k]) * rstd));
+            z[m * K + k] = orc_f64_to_bf16((double)orc_bf16_to_f32(gamma[k]) * t);
+        }
+    }
+}
+
+/* The gated MLP activation in front of down_proj (same card: the
+ * mlp.{gate,up,down}_proj linears): z[m,i] = bf16(SiLU(g) * u) with
+ * SiLU(g) = g / (1 + exp(-g)), g = gate_up[m, i], u = gate_up[m, I + i]:
+ * the gate and up halves of one row of the fused gate/up projection's output
+ * ([M, 2I], gate first).  Evaluated in fp64, rounded once. */
+void orc_silu_mul_bf16(const uint16_t *gate_up, int64_t M, int64_t I, uint16_t *z)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = gate_up + m * 2 * I;
+        for (int64_t i = 0; i < I; ++i) {
+            const double g = (double)orc_bf16_to_f32(row[i]);
+            const double u = (double)orc_bf16_to_f32(row[I + i]);
+            z[m * I + i] = orc_f64_to_bf16(g / (1.0 + exp(-g)) * u);
+        }
+    }
+}

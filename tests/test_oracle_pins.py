@@ -466,3 +466,121 @@ def test_w8a16_fp64_invariant(oracle_lib, gs):
     assert np.allclose(out["y64"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
     assert np.all(np.abs(out["y_f32"].astype(np.float64) - out["y64"]) <= out["bound"])
     assert np.array_equal(out["y_bf16"], bf16_of(out["y_f32"]))
+
+
+# ------------------------------------------------------------ fused producers
+
+def _bf16_value(bits: int) -> Fraction:
+    """Exact value of a finite bf16 bit pattern."""
+    return Fraction(float(np.array([int(bits) << 16], np.uint32).view(np.float32)[0]))
+
+
+def _round_bf16_brute(v: Fraction) -> int:
+    """Nearest bf16 to an exact rational (ties to the even pattern), found by
+    testing the neighbours of torch's rounding of the nearest float32."""
+    approx = int(bf16_of([float(v)])[0])
+    best = None
+    for b in (approx - 1, approx, approx + 1):
+        if b < 0 or (b & 0x7F80) == 0x7F80:
+            continue
+        if (b >> 15) != (approx >> 15) and v != 0:
+            continue
+        d = abs(_bf16_value(b) - v)
+        if best is None or d < best[0] or (d == best[0] and b % 2 == 0):
+            best = (d, b)
+    return best[1]
+
+
+def test_f64_to_bf16_matches_exact_rounding(oracle_lib):
+    rng = np.random.default_rng(11)
+    vals = list(rng.standard_normal(3000) * np.exp(rng.uniform(-60, 60, 3000)))
+    # doubles just off bf16 ties, which a double rounding through fp32 would get wrong
+    for base in (1.0, 1.5, 3.0, 0.8125, 1e-20, 7e30):
+        m, e = np.frexp(base)
+        ulp = 2.0 ** (e - 8)
+        tie = (np.floor(base / ulp) + 0.5) * ulp
+        vals += [tie, tie + tie * 2 ** -40, tie - tie * 2 ** -40, -tie]
+    for v in vals:
+        got = oracle_lib.f64_to_bf16(float(v))
+        assert got == _round_bf16_brute(Fraction(float(v))), (v, hex(got))
+    assert oracle_lib.f64_to_bf16(0.0) == 0 and oracle_lib.f64_to_bf16(-0.0) == 0x8000
+    assert oracle_lib.f64_to_bf16(1e39) == 0x7F80 and oracle_lib.f64_to_bf16(-1e39) == 0xFF80
+
+
+def test_rmsnorm_constant_rows_give_gamma(oracle_lib):
+    """x = c on a whole row: mean x^2 = c^2, so z = gamma exactly (eps = 0)."""
+    K = 256
+    cs = [3.0, -0.15625, 1024.0, 2.0 ** -20]
+    x = np.stack([bf16_of(np.full(K, c)) for c in cs])
+    g = bf16_of(np.linspace(-2.0, 2.0, K))
+    z = oracle_lib.rmsnorm_bf16(x, g, 0.0)
+    for i, c in enumerate(cs):
+        want = g if c > 0 else g ^ np.uint16(0x8000)
+        nz = g != 0
+        assert np.array_equal(z[i][nz], want[nz]), c
+
+
+def test_rmsnorm_hand_row(oracle_lib):
+    """[3, 4, 0, 0]: mean of squares 25/4, rstd = 2/5, t = (6/5, 8/5, 0, 0)."""
+    x = bf16_of([3.0, 4.0, 0.0, 0.0])[None, :]
+    g = bf16_of([1.0, 2.0, 0.5, 4.0])
+    z = oracle_lib.rmsnorm_bf16(x, g, 0.0)[0]
+    t0 = _round_bf16_brute(Fraction(6, 5))
+    t1 = _round_bf16_brute(Fraction(8, 5))
+    assert z[0] == _round_bf16_brute(_bf16_value(t0))
+    assert z[1] == _round_bf16_brute(2 * _bf16_value(t1))
+    assert z[2] == 0 and z[3] == 0
+
+
+def test_rmsnorm_eps_under_the_root(oracle_lib):
+    """K = 1, x = 1, eps = 3: 1 / sqrt(1 + 3) = 1/2; an all-zero row stays 0."""
+    g = bf16_of([3.0])
+    z = oracle_lib.rmsnorm_bf16(bf16_of([[1.0], [0.0]]), g, 3.0)
+    assert z[0, 0] == bf16_of([1.5])[0] and z[1, 0] == 0
+
+
+def test_rmsnorm_power_of_two_scale_invariance(oracle_lib):
+    x = synth.activations(3, "pins/rms", 6, 640, "outliers")
+    g = synth.bf16_bits(1.0 + 0.1 * synth.normal(3, "pins/rms/g", (640,)))
+    z = oracle_lib.rmsnorm_bf16(x, g, 0.0)
+    for j in (-7, 3, 20):
+        xs = bf16_of(synth.bf16_values(x) * np.float32(2.0 ** j))
+        assert np.array_equal(oracle_lib.rmsnorm_bf16(xs, g, 0.0), z)
+
+
+def test_silu_mul_hand_values_and_layout(oracle_lib):
+    """Row [gate | up] = [1, 0, -30, 30 | 2, 5, 1, 3]."""
+    gu = bf16_of([1.0, 0.0, -30.0, 30.0, 2.0, 5.0, 1.0, 3.0])[None, :]
+    z = oracle_lib.silu_mul_bf16(gu)[0]
+    e1 = Fraction(np.exp(-1.0))
+    assert z[0] == _round_bf16_brute(2 / (1 + e1))
+    assert z[1] == 0
+    e30 = Fraction(np.exp(-30.0))
+    assert z[2] == _round_bf16_brute(Fraction(-30) / (1 + 1 / e30))
+    assert z[3] == bf16_of([90.0])[0]      # SiLU(30) = 30 - 2.8e-12 -> 30, times 3
+
+
+def test_silu_odd_identity(oracle_lib):
+    """SiLU(g) - SiLU(-g) = g: with up = 1 the two rounded outputs differ by g
+    up to their roundings."""
+    gs = np.linspace(-12.0, 12.0, 97)
+    gate = bf16_of(gs)
+    g_vals = synth.bf16_values(gate).astype(np.float64)
+    gu_pos = np.concatenate([gate, bf16_of(np.ones_like(gs))])[None, :]
+    gu_neg = np.concatenate([gate ^ np.uint16(0x8000), bf16_of(np.ones_like(gs))])[None, :]
+    zp = synth.bf16_values(oracle_lib.silu_mul_bf16(gu_pos)[0]).astype(np.float64)
+    zn = synth.bf16_values(oracle_lib.silu_mul_bf16(gu_neg)[0]).astype(np.float64)
+    tol = 2.0 ** -8 * (np.abs(zp) + np.abs(zn)) + 1e-30
+    assert np.all(np.abs(zp - zn - g_vals) <= tol)
+
+
+def test_fused_producers_compose_with_act_quant(oracle_lib):
+    x = synth.activations(4, "pins/fp", 5, 384, "normal")
+    g = synth.bf16_bits(1.0 + 0.1 * synth.normal(4, "pins/fp/g", (384,)))
+    q, s, z = oracle_lib.rmsnorm_act_quant_i8(x, g, 1e-6)
+    q2, s2 = oracle_lib.act_quant_i8(z)
+    assert np.array_equal(q, q2) and np.array_equal(s, s2)
+    gu = synth.activations(4, "pins/fp/gu", 5, 2 * 384, "normal")
+    q, s, z = oracle_lib.silu_mul_act_quant_i8(gu)
+    q2, s2 = oracle_lib.act_quant_i8(z)
+    assert np.array_equal(q, q2) and np.array_equal(s, s2) and z.shape == (5, 384)
