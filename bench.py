@@ -86,6 +86,8 @@ WORKLOAD_DESC = {
     "prefill": "W8A8 GS128 gate/up 5120->17408 + down 17408->5120, M in {128,512,2048,8192}",
     "vocab": "W8A8 GS128 vocab head 5120->248320, M in {8,96}",
     "vocab_argmax": "W8A8 GS128 vocab head 5120->248320 with fused greedy argmax, M in {8,96}",
+    "producers": "fused producers + per-token INT8 act-quant: RMSNorm over [M,5120] and "
+                 "SiLU(gate)*up over [M,2x17408], M in {8,96,2048,8192}",
 }
 
 
@@ -521,6 +523,243 @@ def run_ours(args, rank, world, local_rank):
     return line, runner
 
 
+# ------------------------------------------- fused producers (RMSNorm, SiLU*up)
+
+PRODUCER_MS = (8, 96, 2048, 8192)
+PRODUCER_HIDDEN, PRODUCER_INTER, PRODUCER_EPS = 5120, 17408, 1e-6
+
+
+def producer_specs():
+    """(kind, M, K): K is the quantized row length (the hidden size for the
+    norm, the intermediate size for SiLU(gate)*up)."""
+    return [(kind, M, PRODUCER_HIDDEN if kind == "rmsnorm" else PRODUCER_INTER)
+            for M in PRODUCER_MS for kind in ("rmsnorm", "silu_mul")]
+
+
+def producer_bytes(kind, M, K):
+    """Algorithmic bytes of one call: the bf16 input (and the norm weight),
+    the int8 output and the fp32 scales."""
+    read = 2 * M * K + 2 * K if kind == "rmsnorm" else 2 * M * 2 * K
+    return read + M * K + 4 * M
+
+
+_PRODUCER_INPUTS = {}
+
+
+def producer_inputs(kind, M, K, seed=0):
+    key = (kind, M, K, seed)
+    if key not in _PRODUCER_INPUTS:
+        _PRODUCER_INPUTS[key] = _make_producer_inputs(kind, M, K, seed)
+    return _PRODUCER_INPUTS[key]
+
+
+PRODUCER_DISTINCT_ROWS = 64   # rows repeat with this period (input generation time)
+
+
+def _make_producer_inputs(kind, M, K, seed):
+    from w4a16_linear_layers_gb300 import synth
+
+    r = min(M, PRODUCER_DISTINCT_ROWS)
+    reps = (M + r - 1) // r
+    if kind == "rmsnorm":
+        x = synth.activations(seed, f"producers/rms/M{M}", r, K, "outliers")
+        g = synth.bf16_bits(1.0 + 0.1 * synth.normal(seed, "producers/rms/gamma", (K,)))
+        return np.ascontiguousarray(np.tile(x, (reps, 1))[:M]), g
+    x = synth.activations(seed, f"producers/silu/M{M}", r, 2 * K, "normal2")
+    return np.ascontiguousarray(np.tile(x, (reps, 1))[:M]), None
+
+
+def profiled_producer_traffic():
+    """DRAM bytes of the dominant producer launch from the committed ncu
+    summary, or None when act_quant.cu changed since that capture."""
+    import hashlib
+    with open(os.path.join(ROOT, "w4a16_linear_layers_gb300", "csrc", "act_quant.cu"), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    try:
+        with open(os.path.join(ROOT, "profiles", "producers_rmsnorm_silu_quant.md")) as f:
+            text = f.read()
+    except OSError:
+        return None
+    if h not in text:
+        return None
+    for line in text.splitlines():
+        if line.startswith("traffic_bytes_per_launch_top:"):
+            return int(line.split(":")[1])
+    return None
+
+
+def run_producers(args, rank, world, local_rank):
+    import torch
+    from w4a16_linear_layers_gb300 import build as qbuild
+    from w4a16_linear_layers_gb300 import qlin
+
+    qbuild.build()
+    device = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(device)
+    specs = producer_specs()
+    calls = []
+    for kind, M, K in specs:
+        x, g = producer_inputs(kind, M, K)
+        xd = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        gd = None if g is None else torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).to(device)
+        q = torch.empty((M, K), dtype=torch.int8, device=device)
+        sa = torch.empty((M,), dtype=torch.float32, device=device)
+        calls.append((kind, M, K, xd, gd, q, sa))
+
+    def one(c):
+        kind, M, K, xd, gd, q, sa = c
+        if kind == "rmsnorm":
+            qlin.rmsnorm_act_quant_i8(xd, gd, PRODUCER_EPS, q=q, s_a=sa)
+        else:
+            qlin.silu_mul_act_quant_i8(xd, q=q, s_a=sa)
+
+    def capture(cs):
+        st = torch.cuda.Stream(device)
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            for c in cs:
+                one(c)
+        torch.cuda.current_stream().wait_stream(st)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for c in cs:
+                one(c)
+        torch.cuda.synchronize()
+        return gr
+
+    step_graph = capture(calls)
+    # the dominant launch: SiLU(gate)*up at the largest M
+    top = max(calls, key=lambda c: producer_bytes(c[0], c[1], c[2]))
+    top_graph = capture([top])
+    for _ in range(args.warmup):
+        step_graph.replay()
+    torch.cuda.synchronize()
+    if qlin.device_status() != qlin.QLIN_OK:
+        raise SystemExit("device status after warm-up is not OK")
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t_step = time_graph(torch, step_graph, args.steps)
+    t_top = time_graph(torch, top_graph, args.steps)
+    clock_info = clocks.stop()
+
+    host_in = [c[3].cpu().pin_memory() for c in calls]
+    host_q = [torch.empty(c[5].shape, dtype=torch.int8, pin_memory=True) for c in calls]
+    host_s = [torch.empty(c[6].shape, dtype=torch.float32, pin_memory=True) for c in calls]
+    h2d = sum(h.numel() * 2 for h in host_in)
+    d2h = sum(h.numel() for h in host_q) + sum(h.numel() * 4 for h in host_s)
+
+    def e2e_step():
+        for h, c in zip(host_in, calls):
+            c[3].copy_(h, non_blocking=True)
+        for c in calls:
+            one(c)
+        for hq, hs, c in zip(host_q, host_s, calls):
+            hq.copy_(c[5], non_blocking=True)
+            hs.copy_(c[6], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        e2e_step()
+    torch.cuda.synchronize()
+    t_e2e = (time.perf_counter() - t0) / reps
+    if qlin.device_status() != qlin.QLIN_OK:
+        raise SystemExit("device status after timing is not OK")
+    if rank != 0:
+        return None
+    step_bytes = sum(producer_bytes(k, M, K) for k, M, K in specs)
+    top_bytes = producer_bytes(top[0], top[1], top[2])
+    hbm, _, peak_src = measured_peaks()
+    top_s = t_top / args.steps
+    achieved = top_bytes / top_s / 1e9
+    return {
+        "metric": "fused producer + INT8 act-quant GB/s (algorithmic bytes); % of HBM roofline",
+        "value": round(step_bytes * args.steps * world / t_step / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 in, fp32 producer arithmetic, int8 + fp32 scale out",
+        "data": "synthetic (seeded splitmix64; N(0,1) rows with outlier channels, "
+                "N(0,2) gate/up pre-activations, norm weight 1 + N(0, 0.01); "
+                f"rows repeat with period {PRODUCER_DISTINCT_ROWS})",
+        "config": {
+            "workload": WORKLOAD_DESC["producers"],
+            "calls_per_step": len(calls),
+            "bytes_per_step": step_bytes,
+            "l2": "inputs larger than L2: one step moves about 0.9 GB",
+            "timing": "CUDA graph of one step, CUDA events on the replay stream",
+            "parallelism": f"replicas x{world}",
+        },
+        "gpu_launches": len(calls) * args.steps,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": f"producer_quant_kernel<SiLU*up> (M={top[1]}, I={top[2]})",
+            "achieved": round(achieved, 1),
+            "peak": hbm,
+            "peak_source": peak_src,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm, 4),
+            "traffic": profiled_producer_traffic(),
+            "bytes_per_launch": top_bytes,
+            "avg_launch_us": round(top_s * 1e6, 3),
+        },
+        "e2e": {
+            "value": round(step_bytes * world / t_e2e / 1e9, 2),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(t_e2e * 1e3, 4),
+        },
+        "clocks": clock_info,
+    }
+
+
+def producer_oracle_sample(budget_s, seed=0):
+    """The oracle on the whole step (every row of every call), repeated while
+    the time stays under half the budget, on all host cores (one thread per
+    row slice).  Returns (algorithmic bytes covered, seconds, threads, text)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    oracle.build()
+    nthreads = cores()
+    specs = producer_specs()
+    tasks, step_bytes = [], 0
+    for kind, M, K in specs:
+        x, g = producer_inputs(kind, M, K, seed)
+        step_bytes += producer_bytes(kind, M, K)
+        for sl in np.array_split(np.arange(M), min(nthreads, M)):
+            if sl.size:
+                tasks.append((kind, np.ascontiguousarray(x[sl]), g))
+
+    def work(kind, x, g):
+        if kind == "rmsnorm":
+            oracle.rmsnorm_act_quant_i8(x, g, PRODUCER_EPS)
+        else:
+            oracle.silu_mul_act_quant_i8(x)
+
+    reps, total = 0, 0.0
+    while reps < 5 and (reps == 0 or total < 0.5 * budget_s):
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(nthreads) as ex:
+            list(ex.map(lambda t: work(*t), tasks))
+        total += time.perf_counter() - t0
+        reps += 1
+    return step_bytes * reps, total, nthreads, (
+        f"oracle on the whole step ({len(specs)} calls, every row), {reps} time(s), "
+        f"{nthreads} threads")
+
+
 # ------------------------------------------------------------ oracle (CPU)
 
 def cores():
@@ -594,9 +833,36 @@ def oracle_sample(specs, budget_s, seed=0, cache=None):
     return b, t, nthreads, desc
 
 
+def run_reference_producers(args):
+    for _ in range(args.warmup):
+        producer_oracle_sample(1.0)
+    tot_b, tot_t, thr, desc = 0, 0.0, 1, ""
+    for _ in range(args.steps):
+        b, t, thr, desc = producer_oracle_sample(max(1.0, 30.0 / max(1, args.steps)))
+        tot_b += b
+        tot_t += t
+    value = tot_b / tot_t / 1e9
+    return {
+        "impl": "reference",
+        "metric": "fused producer + INT8 act-quant GB/s (algorithmic bytes); % of HBM roofline",
+        "value": round(value, 6), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp64 producer arithmetic, fp32 act-quant (CPU oracle)",
+        "data": "synthetic (seeded splitmix64)",
+        "config": {"workload": WORKLOAD_DESC["producers"]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": thr,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
+    if args.workload == "producers":
+        return run_reference_producers(args)
     specs = workload_specs(args.workload)
     per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     cache = {}
@@ -664,7 +930,16 @@ def main():
 
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    out = run_ours(args, rank, world, local_rank)
+    if args.workload == "producers":
+        line = run_producers(args, rank, world, local_rank)
+        if line is not None:
+            b, t, thr, desc = producer_oracle_sample(args.cpu_budget)
+            line["cpu_baseline"] = {"value": round(b / t / 1e9, 6), "unit": "GB/s", "cores": thr,
+                                    "kind": "oracle", "sample": desc}
+            print(json.dumps(line), flush=True)
+        out = None
+    else:
+        out = run_ours(args, rank, world, local_rank)
     if out is not None:
         line, runner = out
         b, t, thr, desc = oracle_sample(runner.specs, args.cpu_budget)

@@ -88,6 +88,47 @@ qlin_status_t qlin_act_quant_i8(const uint16_t *x, int64_t M, int64_t K,
                                 int8_t *q, float *s_a, qlin_stream_t stream);
 
 /*
+ * The producers of the projections' inputs, fused with the act-quant above:
+ * one read of the producer's input and one write of q and s_a.
+ *
+ * Passages: "Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card, the table of
+ * components kept in BF16 (input_layernorm, post_attention_layernorm: the
+ * RMSNorms in front of the q/k/v and gate/up projections) and the linear-layer
+ * table (mlp.{gate,up,down}_proj: down_proj reads SiLU(gate) * up); the
+ * act-quant passages above.
+ *
+ * qlin_rmsnorm_act_quant_i8, for each row m of x:
+ *   variance = mean_k x[m,k]^2 (fp32),  rstd = 1 / sqrt(variance + eps)
+ *   (IEEE square root and divide),  t = bf16(x * rstd),
+ *   z[m,k] = bf16(gamma[k] * t)  (the decoder norm's bf16 output),
+ * then (q, s_a) = act-quant of z exactly as qlin_act_quant_i8 defines it.
+ *   x      bf16 [M, K]   the residual stream
+ *   gamma  bf16 [K]      the norm's weight
+ *   eps    >= 0, finite
+ *
+ * qlin_silu_mul_act_quant_i8, for each row m of gate_up [M, 2I] (the fused
+ * gate/up projection's output: gate in columns [0, I), up in [I, 2I)):
+ *   z[m,i] = bf16(SiLU(g) * u),  SiLU(g) = g * sigmoid(g) in fp32, the
+ *   sigmoid from e = expf(-|g|) and an approximate divide by 1 + e (within
+ *   2 ulp), g = gate_up[m,i], u = gate_up[m,I+i],
+ * then (q, s_a) = act-quant of z.
+ *
+ *   q    int8 [M, K] (or [M, I])   output
+ *   s_a  fp32 [M]                  output
+ *   y    bf16 [M, K] (or [M, I])   optional output: z itself; NULL skips it
+ *
+ * K (or I) must be a positive multiple of 128; all pointers 16-byte aligned.
+ * Non-finite inputs are outside the contract.
+ */
+qlin_status_t qlin_rmsnorm_act_quant_i8(const uint16_t *x, const uint16_t *gamma, float eps,
+                                        int64_t M, int64_t K, int8_t *q, float *s_a,
+                                        uint16_t *y, qlin_stream_t stream);
+
+qlin_status_t qlin_silu_mul_act_quant_i8(const uint16_t *gate_up, int64_t M, int64_t I,
+                                         int8_t *q, float *s_a, uint16_t *y,
+                                         qlin_stream_t stream);
+
+/*
  * W8A8 GS128 linear:  y = bf16( s_a[m] * sum_g s_w[g,n] * P[g,m,n] ),
  * P[g,m,n] = sum_{k = 128g}^{128g+127} q_a[m,k] * q_w[k,n]  (exact integers).
  *

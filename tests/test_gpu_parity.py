@@ -52,6 +52,23 @@ def test_act_quant_bit_exact(M, K, kind):
     assert np.array_equal(q, oq)
 
 
+def test_act_quant_dense_sweep_near_rounding_boundaries():
+    """Every row holds its maximum and 4095 bf16 values spread over
+    [-amax, amax]: many quotients x / s land next to a half-integer, where the
+    kernel's reciprocal shortcut must hand over to the IEEE divide."""
+    rng = np.random.default_rng(7)
+    M, K = 64, 4096
+    amax = np.exp(rng.uniform(np.log(1e-3), np.log(1e3), M)).astype(np.float32)
+    amax = synth.bf16_values(synth.bf16_bits(amax))
+    x = np.linspace(-1.0, 1.0, K, dtype=np.float64)[None, :] * amax[:, None]
+    x[:, 0] = amax
+    xb = synth.bf16_bits(x)
+    q, s = _act_quant_gpu(xb)
+    oq, os_ = oracle.act_quant_i8(xb)
+    assert np.array_equal(s.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(q, oq)
+
+
 def test_act_quant_ties_and_divide_cases():
     rows = [
         [127, 2.5, -3.5, 0.5, 1.5, -0.5, -1.5, 126.5],
@@ -472,3 +489,82 @@ def test_repeated_launches_are_identical(fmt, M, K, N):
     qlin.device_status()
     assert st == qlin.QLIN_OK, f"{qlin.status_string(st)} (wait {where}, block {block})"
     assert int(mismatches) == 0
+
+
+# ------------------------------------------- fused producers + act-quant
+
+def _bf16_steps_apart(a_bits, b_bits):
+    """Distance in bf16 steps between two bit-pattern arrays (+0 and -0 equal)."""
+    def ordered(b):
+        b = b.astype(np.int64)
+        return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+def _check_producer(q_d, s_d, y_d, z_ref, what, max_steps=1, gamma=None):
+    """The kernel's bf16 producer output z may differ from the oracle's (fp32
+    vs fp64 evaluation) where a value sits at a bf16 rounding boundary,
+    rarely: by one step where z is rounded once (SiLU(gate) * up); by up to
+    two for the norm.  There the intermediate t = bf16(x * rstd) can flip by
+    one step, which moves gamma * t by D = |gamma| * ulp(t) / ulp(z) steps of
+    z before z is rounded; D < 2 whenever 1/2 < |gamma| < 2, and two
+    roundings of values D < 2 apart land at most two steps apart.  The
+    act-quant of the kernel's own z is then exact."""
+    y = from_dev_bits(y_d)
+    d = _bf16_steps_apart(y, z_ref)
+    assert d.max() <= max_steps, f"{what}: producer output off by {d.max()} bf16 steps"
+    if gamma is not None and d.max() > 1:
+        two = np.nonzero(d > 1)
+        gk = np.abs(synth.bf16_values(gamma)[two[1]])
+        assert np.all((gk > 0.5) & (gk < 2.0)), what
+    assert (d > 0).mean() <= 1e-3, f"{what}: {(d > 0).mean():.2e} of outputs off by one step"
+    q_ref, s_ref = oracle.act_quant_i8(y)
+    assert np.array_equal(q_d.cpu().numpy(), q_ref), what
+    assert np.array_equal(s_d.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), what
+
+
+@pytest.mark.parametrize("M,K,kind", [(1, 128, "normal"), (8, 5120, "outliers"), (96, 5120, "normal2"),
+                                      (130, 640, "outliers"), (2048, 5120, "outliers"),
+                                      (3, 40960, "normal")])
+def test_rmsnorm_act_quant_matches_oracle(M, K, kind):
+    x = synth.activations(30, f"gpu/rms/{M}/{K}", M, K, kind)
+    if M > 2:
+        x[M // 2] = 0          # an all-zero row: z = 0, s_a = 0, q = 0
+    g = synth.bf16_bits(1.0 + 0.1 * synth.normal(30, f"gpu/rms/{K}/gamma", (K,)))
+    eps = 1e-6
+    xd, gd = to_dev_bits(x, torch.bfloat16), to_dev_bits(g, torch.bfloat16)
+    y = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    q, s = qlin.rmsnorm_act_quant_i8(xd, gd, eps, y=y)
+    q2, s2 = qlin.rmsnorm_act_quant_i8(xd, gd, eps)           # without the bf16 output
+    torch.cuda.synchronize()
+    _check_producer(q, s, y, oracle.rmsnorm_bf16(x, g, eps), f"rmsnorm {M}x{K}", max_steps=2,
+                    gamma=g)
+    assert torch.equal(q, q2) and torch.equal(s, s2)
+
+
+@pytest.mark.parametrize("M,I", [(1, 128), (8, 17408), (96, 17408), (130, 384), (512, 17408),
+                                 (2, 34816)])
+def test_silu_mul_act_quant_matches_oracle(M, I):
+    gu = synth.activations(31, f"gpu/silu/{M}/{I}", M, 2 * I, "normal2")
+    if M > 2:
+        gu[M // 2, :I] = 0     # SiLU(0) = 0: an all-zero output row
+    gud = to_dev_bits(gu, torch.bfloat16)
+    y = torch.empty((M, I), dtype=torch.bfloat16, device="cuda")
+    q, s = qlin.silu_mul_act_quant_i8(gud, y=y)
+    q2, s2 = qlin.silu_mul_act_quant_i8(gud)
+    torch.cuda.synchronize()
+    _check_producer(q, s, y, oracle.silu_mul_bf16(gu), f"silu_mul {M}x{I}")
+    assert torch.equal(q, q2) and torch.equal(s, s2)
+
+
+def test_fused_producers_reject_bad_shapes():
+    x = torch.zeros((4, 200), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones((200,), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(qlin.QlinError):
+        qlin.rmsnorm_act_quant_i8(x, g, 1e-6)                 # K not a multiple of 128
+    x = torch.zeros((4, 256), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones((256,), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(qlin.QlinError):
+        qlin.rmsnorm_act_quant_i8(x, g, -1.0)                 # negative eps
+    with pytest.raises(qlin.QlinError):
+        qlin.silu_mul_act_quant_i8(torch.zeros((4, 200), dtype=torch.bfloat16, device="cuda"))

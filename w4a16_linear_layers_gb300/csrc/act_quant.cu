@@ -13,6 +13,8 @@
 // (div.rn), exactly as the format defines them, and written as 8-byte stores.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "qlin_device.cuh"
 #include "qlin_internal.h"
 
@@ -50,6 +52,28 @@ __device__ __forceinline__ uint2 quant8(uint4 v, float s) {
         (quant1(bf16_lo(v.y), s) << 16) | (quant1(bf16_hi(v.y), s) << 24);
   o.y = quant1(bf16_lo(v.z), s) | (quant1(bf16_hi(v.z), s) << 8) |
         (quant1(bf16_lo(v.w), s) << 16) | (quant1(bf16_hi(v.w), s) << 24);
+  return o;
+}
+
+// The same code from the reciprocal y = 1/s (correctly rounded) instead of a
+// divide per element.  t = x * y is within 2^-16 of x / s for |x / s| <= 127,
+// so when t is further than 2^-15 from a half-integer, the IEEE quotient
+// rounds to the same integer as t; the rare values near a rounding boundary
+// take the IEEE divide.  The codes are those of quant1 in every case.
+__device__ __forceinline__ uint32_t quant1y(float x, float s, float y) {
+  const float t = __fmul_rn(x, y);
+  float r = rintf(t);
+  if (fabsf(__fsub_rn(t, r)) > 0.5f - 0x1p-15f) r = rintf(__fdiv_rn(x, s));
+  r = fminf(fmaxf(r, -127.0f), 127.0f);
+  return static_cast<uint32_t>(static_cast<int>(r)) & 0xFFu;
+}
+
+__device__ __forceinline__ uint2 quant8y(uint4 v, float s, float y) {
+  uint2 o;
+  o.x = quant1y(bf16_lo(v.x), s, y) | (quant1y(bf16_hi(v.x), s, y) << 8) |
+        (quant1y(bf16_lo(v.y), s, y) << 16) | (quant1y(bf16_hi(v.y), s, y) << 24);
+  o.y = quant1y(bf16_lo(v.z), s, y) | (quant1y(bf16_hi(v.z), s, y) << 8) |
+        (quant1y(bf16_lo(v.w), s, y) << 16) | (quant1y(bf16_hi(v.w), s, y) << 24);
   return o;
 }
 
@@ -97,18 +121,390 @@ __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint16_t* _
     for (int64_t v = tid; v < nvec; v += kAqThreads) qrow[v] = make_uint2(0u, 0u);
     return;
   }
+  const float y = __frcp_rn(s);
   if (kCached) {
 #pragma unroll
     for (int i = 0; i < kAqVecPerThread; ++i) {
       const int64_t v = tid + static_cast<int64_t>(i) * kAqThreads;
-      if (v < nvec) qrow[v] = quant8(cache[i], s);
+      if (v < nvec) qrow[v] = quant8y(cache[i], s, y);
     }
   } else {
-    for (int64_t v = tid; v < nvec; v += kAqThreads) qrow[v] = quant8(__ldg(row + v), s);
+    for (int64_t v = tid; v < nvec; v += kAqThreads) qrow[v] = quant8y(__ldg(row + v), s, y);
   }
 }
 
+// ------------------------------------------------------ fused producers
+//
+// The kernels that produce a linear's input, fused with its act-quant: one
+// read of the producer's input and one write of q and s_a, instead of a bf16
+// round trip through memory between the producer and act-quant.  The
+// producer's bf16 output z is formed exactly as the unfused producer would
+// store it, and quantized exactly as act_quant_kernel does; it is also
+// written out when y is not null.
+
+// Sum over the block (every thread gets the result).  `red` is reused by the
+// next reduction only after the barrier at the start of the next call.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = red[0];
+#pragma unroll
+  for (int w = 1; w < kAqThreads / 32; ++w) t += red[w];
+  return t;
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = red[0];
+#pragma unroll
+  for (int w = 1; w < kAqThreads / 32; ++w) t = fmaxf(t, red[w]);
+  return t;
+}
+
+__device__ __forceinline__ float sumsq8(uint4 v, float acc) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = __fmaf_rn(bf16_lo(w[i]), bf16_lo(w[i]), acc);
+    acc = __fmaf_rn(bf16_hi(w[i]), bf16_hi(w[i]), acc);
+  }
+  return acc;
+}
+
+// RMSNorm output of 8 elements: t = bf16(x * rstd), z = bf16(gamma * t)
+// (the product of two bf16 values is exact in fp32, so z is rounded once).
+__device__ __forceinline__ uint32_t norm2(uint32_t x, uint32_t g, float rstd) {
+  const uint32_t t = bf16x2_rn(__fmul_rn(bf16_lo(x), rstd), __fmul_rn(bf16_hi(x), rstd));
+  return bf16x2_rn(__fmul_rn(bf16_lo(g), bf16_lo(t)), __fmul_rn(bf16_hi(g), bf16_hi(t)));
+}
+
+__device__ __forceinline__ uint4 norm8(uint4 x, uint4 g, float rstd) {
+  return make_uint4(norm2(x.x, g.x, rstd), norm2(x.y, g.y, rstd), norm2(x.z, g.z, rstd),
+                    norm2(x.w, g.w, rstd));
+}
+
+// SiLU(g) * u of 8 elements in fp32, rounded once to bf16: SiLU(g) =
+// g * sigmoid(g), the sigmoid from e = exp(-|g|) <= 1 (1 / (1 + e) for g >= 0,
+// e / (1 + e) below), so the divisor stays in [1, 2] and the approximate
+// divide (within 2 ulp there) never meets an overflowing exponential.
+__device__ __forceinline__ float silu_mul1(float g, float u) {
+  const float e = expf(-fabsf(g));
+  const float sig = __fdividef(g >= 0.0f ? 1.0f : e, __fadd_rn(1.0f, e));
+  return __fmul_rn(__fmul_rn(g, sig), u);
+}
+
+__device__ __forceinline__ uint32_t silu_mul2(uint32_t g, uint32_t u) {
+  return bf16x2_rn(silu_mul1(bf16_lo(g), bf16_lo(u)), silu_mul1(bf16_hi(g), bf16_hi(u)));
+}
+
+__device__ __forceinline__ uint4 silu_mul8(uint4 g, uint4 u) {
+  return make_uint4(silu_mul2(g.x, u.x), silu_mul2(g.y, u.y), silu_mul2(g.z, u.z),
+                    silu_mul2(g.w, u.w));
+}
+
+// Rows longer than the persistent form holds (more than 32768 elements): one
+// block per row, the row read from memory on each pass (the second and third
+// from L2).  The norm: variance (fp32, per-thread fma chains then the block
+// sum), rstd = 1 / sqrt(variance + eps) with IEEE square root and divide, z,
+// then act-quant of z.
+__global__ void __launch_bounds__(kAqThreads) rmsnorm_quant_long_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps, int64_t K,
+    int8_t* __restrict__ q, float* __restrict__ s_out, uint16_t* __restrict__ y) {
+  __shared__ float red[kAqThreads / 32];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int64_t m = blockIdx.x;
+  const int64_t nvec = K / 8;
+  const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
+  const uint4* grow = reinterpret_cast<const uint4*>(gamma);
+  uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
+  uint4* yrow = y ? reinterpret_cast<uint4*>(y + m * K) : nullptr;
+  const int tid = threadIdx.x;
+  float ss = 0.0f;
+  for (int64_t v = tid; v < nvec; v += kAqThreads) ss = sumsq8(__ldg(row + v), ss);
+  ss = block_sum(ss, red);
+  const float rstd =
+      __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps)));
+  float amax = 0.0f;
+  for (int64_t v = tid; v < nvec; v += kAqThreads) {
+    const uint4 z = norm8(__ldg(row + v), __ldg(grow + v), rstd);
+    amax = absmax8(z, amax);
+    if (yrow) yrow[v] = z;
+  }
+  amax = block_max(amax, red);
+  const float s = __fdiv_rn(amax, 127.0f);
+  if (tid == 0) s_out[m] = s;
+  for (int64_t v = tid; v < nvec; v += kAqThreads)
+    qrow[v] = amax == 0.0f ? make_uint2(0u, 0u)
+                           : quant8(norm8(__ldg(row + v), __ldg(grow + v), rstd), s);
+}
+
+// The same for SiLU(gate) * up rows of more than 32768 elements.
+__global__ void __launch_bounds__(kAqThreads) silu_mul_quant_long_kernel(
+    const uint16_t* __restrict__ gate_up, int64_t I, int8_t* __restrict__ q,
+    float* __restrict__ s_out, uint16_t* __restrict__ y) {
+  __shared__ float red[kAqThreads / 32];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int64_t m = blockIdx.x;
+  const int64_t nvec = I / 8;
+  const uint4* grow = reinterpret_cast<const uint4*>(gate_up + m * 2 * I);
+  const uint4* urow = grow + nvec;
+  uint2* qrow = reinterpret_cast<uint2*>(q + m * I);
+  uint4* yrow = y ? reinterpret_cast<uint4*>(y + m * I) : nullptr;
+  const int tid = threadIdx.x;
+  float amax = 0.0f;
+  for (int64_t v = tid; v < nvec; v += kAqThreads) {
+    const uint4 z = silu_mul8(__ldg(grow + v), __ldg(urow + v));
+    amax = absmax8(z, amax);
+    if (yrow) yrow[v] = z;
+  }
+  amax = block_max(amax, red);
+  const float s = __fdiv_rn(amax, 127.0f);
+  if (tid == 0) s_out[m] = s;
+  for (int64_t v = tid; v < nvec; v += kAqThreads)
+    qrow[v] = amax == 0.0f ? make_uint2(0u, 0u) : quant8(silu_mul8(__ldg(grow + v), __ldg(urow + v)), s);
+}
+
+// Persistent form for rows that fit on chip (up to 32768 elements): blocks of
+// 1024 threads (rows over 8192 elements; one block per SM) or 256 threads
+// (several blocks per SM) walk rows m = blockIdx.x, + gridDim.x, ...
+// Each row's bf16 input lands in a shared-memory ring by one bulk copy
+// (cp.async.bulk, completion on an mbarrier), issued `stages` rows ahead, so
+// the next rows stream in while this one is reduced, quantized and stored.
+// A ring slot is refilled as soon as every thread has copied its part of the
+// row into registers (the first block-wide reduction's barrier).
+constexpr int kPVec = 4;          // row vectors (8 elements) per thread
+constexpr int kPMaxStages = 4;
+constexpr uint32_t kPSmemBudget = 200u * 1024u;   // 1024-thread blocks
+constexpr uint32_t kPSmemBudgetSmall = 44u * 1024u;   // 256-thread blocks
+enum : int { kProdRms = 0, kProdSilu = 1 };
+
+struct ProducerParams {
+  const uint16_t* in;      // x [M, K] (norm) or gate_up [M, 2K] (SiLU)
+  const uint16_t* gamma;   // norm weight [K]
+  float eps;
+  int64_t M, K;            // K: elements of one quantized row
+  int8_t* q;
+  float* s;
+  uint16_t* y;             // optional bf16 producer output
+  int* err;
+  uint64_t limit_ns;
+  int stages;
+  uint32_t row_bytes;      // input bytes of one row
+};
+
+template <int kThreads>
+__device__ __forceinline__ float block_sum_p(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) t += red[w];
+  return t;
+}
+
+template <int kThreads>
+__device__ __forceinline__ float block_max_p(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) t = fmaxf(t, red[w]);
+  return t;
+}
+
+template <int kKind, int kPThreads>
+__global__ void __launch_bounds__(kPThreads) producer_quant_kernel(const ProducerParams p) {
+  extern __shared__ uint8_t psmem_raw[];
+  __shared__ uint64_t full[kPMaxStages];
+  __shared__ float red[kPThreads / 32];
+  __shared__ int abort_flag;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(psmem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  const uint32_t ring_u32 = smem_u32(ring);
+  const int tid = threadIdx.x;
+  const int stages = p.stages;
+  const int64_t nvec = p.K / 8;
+  const int64_t in_row = kKind == kProdRms ? p.K : 2 * p.K;   // input elements per row
+  const int nrows = static_cast<int>((p.M - blockIdx.x + gridDim.x - 1) / gridDim.x);
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) mbar_init(smem_u32(&full[i]), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // the input comes from the previous kernel, which may also still read q
+  grid_dep_wait();
+  grid_dep_launch();
+  const WaitCtx ctx{p.err, &abort_flag, p.limit_ns};
+  int never_abort = 0;
+  const WaitCtx drain_ctx{p.err, &never_abort, p.limit_ns};
+  auto issue = [&](int i) {   // thread 0: row i of this block into slot i % stages
+    const int64_t m = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+    const uint32_t bar = smem_u32(&full[i % stages]);
+    mbar_arrive_expect_tx(bar, p.row_bytes);
+    bulk_load(ring_u32 + static_cast<uint32_t>(i % stages) * p.row_bytes, p.in + m * in_row,
+              p.row_bytes, bar);
+  };
+  int issued = 0;
+  if (tid == 0) {
+    for (; issued < stages && issued < nrows; ++issued) issue(issued);
+  }
+  const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
+  int done = 0;
+  for (int i = 0; i < nrows; ++i) {
+    const int st = i % stages;
+    const bool ok = mbar_wait(smem_u32(&full[st]), static_cast<uint32_t>(i / stages) & 1u, ctx, 40);
+    if (!__syncthreads_and(ok)) break;
+    const int64_t m = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+    const uint4* srow = reinterpret_cast<const uint4*>(ring + static_cast<uint32_t>(st) * p.row_bytes);
+    uint4 z[kPVec];
+    float amax = 0.0f;
+    if constexpr (kKind == kProdRms) {
+      float ss = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kPVec; ++j) {
+        const int64_t v = tid + static_cast<int64_t>(j) * kPThreads;
+        if (v < nvec) {
+          z[j] = srow[v];
+          ss = sumsq8(z[j], ss);
+        }
+      }
+      ss = block_sum_p<kPThreads>(ss, red);   // every thread has its part of the row in registers
+      if (tid == 0 && issued < nrows) {
+        fence_proxy_async_smem();
+        issue(issued++);
+      }
+      const float rstd =
+          __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(p.K)), p.eps)));
+#pragma unroll
+      for (int j = 0; j < kPVec; ++j) {
+        const int64_t v = tid + static_cast<int64_t>(j) * kPThreads;
+        if (v < nvec) {
+          z[j] = norm8(z[j], __ldg(g4 + v), rstd);
+          amax = absmax8(z[j], amax);
+        }
+      }
+      amax = block_max_p<kPThreads>(amax, red);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPVec; ++j) {
+        const int64_t v = tid + static_cast<int64_t>(j) * kPThreads;
+        if (v < nvec) {
+          z[j] = silu_mul8(srow[v], srow[nvec + v]);
+          amax = absmax8(z[j], amax);
+        }
+      }
+      amax = block_max_p<kPThreads>(amax, red);
+      if (tid == 0 && issued < nrows) {
+        fence_proxy_async_smem();
+        issue(issued++);
+      }
+    }
+    const float s = __fdiv_rn(amax, 127.0f);
+    const float y = __frcp_rn(s);
+    if (tid == 0) p.s[m] = s;
+    uint2* qrow = reinterpret_cast<uint2*>(p.q + m * p.K);
+    uint4* yrow = p.y ? reinterpret_cast<uint4*>(p.y + m * p.K) : nullptr;
+#pragma unroll
+    for (int j = 0; j < kPVec; ++j) {
+      const int64_t v = tid + static_cast<int64_t>(j) * kPThreads;
+      if (v < nvec) {
+        qrow[v] = amax == 0.0f ? make_uint2(0u, 0u) : quant8y(z[j], s, y);
+        if (yrow) yrow[v] = z[j];
+      }
+    }
+    done = i + 1;
+  }
+  // a block that gave up waits for the copies it still has in flight
+  if (tid == 0) {
+    for (int j = done; j < issued; ++j)
+      (void)mbar_wait(smem_u32(&full[j % stages]), static_cast<uint32_t>(j / stages) & 1u, drain_ctx,
+                      41);
+  }
+}
+
+template <int kKind, int kThreads>
+cudaError_t launch_producer_t(const ProducerParams& pp_in, int sm_count, cudaStream_t stream) {
+  constexpr uint32_t budget = kThreads == 1024 ? kPSmemBudget : kPSmemBudgetSmall;
+  ProducerParams pp = pp_in;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int per_sm = 1;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(producer_quant_kernel<kKind, kThreads>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(budget + 128));
+    if (attr_err == cudaSuccess)
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, producer_quant_kernel<kKind, kThreads>, kThreads, budget + 128);
+    if (per_sm < 1) per_sm = 1;
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int stages = static_cast<int>(budget / pp.row_bytes);
+  pp.stages = stages > kPMaxStages ? kPMaxStages : stages;
+  const int64_t slots = static_cast<int64_t>(sm_count) * per_sm;
+  const int64_t blocks = pp.M < slots ? pp.M : slots;
+  pp.limit_ns = kWaitLimitNs;
+  return launch_pdl(producer_quant_kernel<kKind, kThreads>, dim3(static_cast<unsigned>(blocks)),
+                    dim3(kThreads), static_cast<size_t>(pp.stages) * pp.row_bytes + 128, stream,
+                    pp);
+}
+
+// Rows of up to 8192 elements take 256-thread blocks (several per SM), up to
+// 32768 elements 1024-thread blocks; longer rows (or rows whose input does
+// not fit the ring) return false.
+template <int kKind>
+bool launch_producer(const ProducerParams& pp, int sm_count, cudaStream_t stream,
+                     cudaError_t* e) {
+  if (pp.K <= 256 * kPVec * 8 && pp.row_bytes <= kPSmemBudgetSmall) {
+    *e = launch_producer_t<kKind, 256>(pp, sm_count, stream);
+    return true;
+  }
+  if (pp.K <= 1024 * kPVec * 8 && pp.row_bytes <= kPSmemBudget) {
+    *e = launch_producer_t<kKind, 1024>(pp, sm_count, stream);
+    return true;
+  }
+  return false;
+}
+
 }  // namespace
+
+cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
+                                 int64_t K, int8_t* q, float* s, uint16_t* y, int* err,
+                                 int sm_count, cudaStream_t stream) {
+  const ProducerParams pp{x, gamma, eps, M, K, q, s, y, err, 0, 0,
+                          static_cast<uint32_t>(K * 2)};
+  cudaError_t e = cudaSuccess;
+  if (K <= 32768 && launch_producer<kProdRms>(pp, sm_count, stream, &e)) return e;
+  return launch_pdl(rmsnorm_quant_long_kernel, dim3(static_cast<unsigned>(M)), dim3(kAqThreads), 0,
+                    stream, x, gamma, eps, K, q, s, y);
+}
+
+cudaError_t launch_silu_mul_quant(const uint16_t* gate_up, int64_t M, int64_t I, int8_t* q,
+                                  float* s, uint16_t* y, int* err, int sm_count,
+                                  cudaStream_t stream) {
+  const ProducerParams pp{gate_up, nullptr, 0.0f, M, I, q, s, y, err, 0, 0,
+                          static_cast<uint32_t>(I * 4)};
+  cudaError_t e = cudaSuccess;
+  if (I <= 32768 && launch_producer<kProdSilu>(pp, sm_count, stream, &e)) return e;
+  return launch_pdl(silu_mul_quant_long_kernel, dim3(static_cast<unsigned>(M)), dim3(kAqThreads), 0,
+                    stream, gate_up, I, q, s, y);
+}
 
 cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s,
                              cudaStream_t stream) {

@@ -1,6 +1,7 @@
 // qlin_api.cu -- the extern "C" entry points of libqlin (include/qlin.h):
 // argument checks, per-device state (SM count, architecture, the device error
 // word) and dispatch to the launchers.  No call allocates device memory.
+#include <cmath>
 #include <mutex>
 
 #include "../../include/qlin.h"
@@ -150,6 +151,39 @@ qlin_status_t qlin_act_quant_i8(const uint16_t* x, int64_t M, int64_t K, int8_t*
   if (st != QLIN_OK) return st;
   if (M == 0) return QLIN_OK;
   return from_cuda(launch_act_quant(x, M, K, q, s_a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_rmsnorm_act_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps,
+                                        int64_t M, int64_t K, int8_t* q, float* s_a, uint16_t* y,
+                                        qlin_stream_t stream) {
+  if (x == nullptr || gamma == nullptr || q == nullptr || s_a == nullptr) return QLIN_ERR_NULL;
+  if (M < 0 || M > kMaxDim || K < kGroup || K > kMaxDim || (K % kGroup) != 0 || !(eps >= 0.0f) ||
+      !std::isfinite(eps))
+    return QLIN_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(gamma) || !aligned16(q) || !aligned16(s_a) ||
+      (y != nullptr && !aligned16(y)))
+    return QLIN_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  qlin_status_t st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  if (M == 0) return QLIN_OK;
+  return from_cuda(launch_rmsnorm_quant(x, gamma, eps, M, K, q, s_a, y, d->err_word, d->sm_count,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qlin_status_t qlin_silu_mul_act_quant_i8(const uint16_t* gate_up, int64_t M, int64_t I, int8_t* q,
+                                         float* s_a, uint16_t* y, qlin_stream_t stream) {
+  if (gate_up == nullptr || q == nullptr || s_a == nullptr) return QLIN_ERR_NULL;
+  if (M < 0 || M > kMaxDim || I < kGroup || I > kMaxDim || (I % kGroup) != 0)
+    return QLIN_ERR_SHAPE;
+  if (!aligned16(gate_up) || !aligned16(q) || !aligned16(s_a) || (y != nullptr && !aligned16(y)))
+    return QLIN_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  qlin_status_t st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  if (M == 0) return QLIN_OK;
+  return from_cuda(launch_silu_mul_quant(gate_up, M, I, q, s_a, y, d->err_word, d->sm_count,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qlin_status_t qlin_gemm_w8a8_gs128(const int8_t* q_a, const float* s_a, const int32_t* qweight,

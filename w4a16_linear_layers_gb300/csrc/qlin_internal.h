@@ -22,6 +22,14 @@ const DeviceInfo* current_device();
 cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s,
                              cudaStream_t stream);
 
+cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
+                                 int64_t K, int8_t* q, float* s, uint16_t* y, int* err,
+                                 int sm_count, cudaStream_t stream);
+
+cudaError_t launch_silu_mul_quant(const uint16_t* gate_up, int64_t M, int64_t I, int8_t* q,
+                                  float* s, uint16_t* y, int* err, int sm_count,
+                                  cudaStream_t stream);
+
 cudaError_t launch_pack(const int8_t* q, int64_t K, int64_t N, int bits, int32_t* qweight,
                         int32_t* qzeros, int* err, cudaStream_t stream);
 

@@ -32,6 +32,8 @@ QLIN_ERR_VALUE_RANGE = -21
 
 EXPORTS = (
     "qlin_act_quant_i8",
+    "qlin_rmsnorm_act_quant_i8",
+    "qlin_silu_mul_act_quant_i8",
     "qlin_gemm_w8a8_gs128",
     "qlin_gemm_w8a8_gs128_noalloc",
     "qlin_gemm_w4a16_g128",
@@ -78,6 +80,8 @@ def load():
         P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
         sig = {
             "qlin_act_quant_i8": ([P, I64, I64, P, P, P], I),
+            "qlin_rmsnorm_act_quant_i8": ([P, P, ctypes.c_float, I64, I64, P, P, P, P], I),
+            "qlin_silu_mul_act_quant_i8": ([P, I64, I64, P, P, P, P], I),
             "qlin_gemm_w8a8_gs128": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_gemm_w8a8_gs128_noalloc": ([P, P, P, P, I64, I64, I64, P, P], I),
             "qlin_gemm_w4a16_g128": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
@@ -149,6 +153,58 @@ def act_quant_i8(x: torch.Tensor, q: torch.Tensor | None = None, s_a: torch.Tens
     _need(q, "q", torch.int8, 2)
     _need(s_a, "s_a", torch.float32, 1)
     _check(load().qlin_act_quant_i8(_ptr(x), M, K, _ptr(q), _ptr(s_a), _stream_handle(stream)))
+    return q, s_a
+
+
+def _quant_outputs(M, K, device, q, s_a):
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.int8, device=device)
+    if s_a is None:
+        s_a = torch.empty((M,), dtype=torch.float32, device=device)
+    _need(q, "q", torch.int8, 2)
+    _need(s_a, "s_a", torch.float32, 1)
+    if tuple(q.shape) != (M, K) or tuple(s_a.shape) != (M,):
+        raise ValueError("q must be [M, K] and s_a [M]")
+    return q, s_a
+
+
+def rmsnorm_act_quant_i8(x: torch.Tensor, gamma: torch.Tensor, eps: float, q=None, s_a=None,
+                         y=None, stream=None):
+    """RMSNorm of x bf16 [M,K] with weight gamma bf16 [K], then per-token INT8
+    act-quant -> (q int8 [M,K], s_a fp32 [M]).  If y (bf16 [M,K]) is given
+    the norm's bf16 output is written there too."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(gamma, "gamma", torch.bfloat16, 1)
+    M, K = x.shape
+    if tuple(gamma.shape) != (K,):
+        raise ValueError("gamma must be [K]")
+    q, s_a = _quant_outputs(M, K, x.device, q, s_a)
+    if y is not None:
+        _need(y, "y", torch.bfloat16, 2)
+        if tuple(y.shape) != (M, K):
+            raise ValueError("y must be [M, K]")
+    _check(load().qlin_rmsnorm_act_quant_i8(_ptr(x), _ptr(gamma), float(eps), M, K, _ptr(q),
+                                            _ptr(s_a), _ptr(y) if y is not None else None,
+                                            _stream_handle(stream)))
+    return q, s_a
+
+
+def silu_mul_act_quant_i8(gate_up: torch.Tensor, q=None, s_a=None, y=None, stream=None):
+    """SiLU(gate) * up of gate_up bf16 [M, 2I] (gate columns first), then
+    per-token INT8 act-quant -> (q int8 [M,I], s_a fp32 [M]).  If y (bf16
+    [M,I]) is given the activation's bf16 output is written there too."""
+    _need(gate_up, "gate_up", torch.bfloat16, 2)
+    M, I2 = gate_up.shape
+    if I2 % 2:
+        raise ValueError("gate_up must have an even number of columns")
+    q, s_a = _quant_outputs(M, I2 // 2, gate_up.device, q, s_a)
+    if y is not None:
+        _need(y, "y", torch.bfloat16, 2)
+        if tuple(y.shape) != (M, I2 // 2):
+            raise ValueError("y must be [M, I]")
+    _check(load().qlin_silu_mul_act_quant_i8(_ptr(gate_up), M, I2 // 2, _ptr(q), _ptr(s_a),
+                                             _ptr(y) if y is not None else None,
+                                             _stream_handle(stream)))
     return q, s_a
 
 
