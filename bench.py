@@ -350,6 +350,25 @@ class LayerRunner:
         return g
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank floats over all ranks (identity
+    without a process group).  Every rank gets the result."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_step, steps, world, seconds):
+    """Throughput of the whole job: every rank processed units_per_step per
+    step (weak scaling), and the job took the slowest rank's time."""
+    return units_per_step * steps * world / seconds
+
+
 def time_graph(torch, graph, reps):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -417,10 +436,7 @@ def run_ours(args, rank, world, local_rank):
     t_gemm = time_graph(torch, gemm_graph, args.steps)
     t_alt = time_graph(torch, alt_graph, args.steps) if alt_graph is not None else 0.0
     clock_info = clocks.stop()
-    if dist:
-        t = torch.tensor([t_step, t_gemm, t_alt], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, t_gemm, t_alt = t.tolist()
+    t_step, t_gemm, t_alt = max_over_ranks([t_step, t_gemm, t_alt], device)
 
     # end to end through the binding: inputs copied from pinned host memory,
     # outputs copied back, every step, no graph
@@ -446,10 +462,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     torch.cuda.synchronize()
     t_e2e = (time.perf_counter() - t0) / e2e_reps
-    if dist:
-        t = torch.tensor([t_e2e], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_e2e = t.item()
+    t_e2e, = max_over_ranks([t_e2e], device)
     st, where, block = qlin.device_error_detail()
     if st != qlin.QLIN_OK:
         raise SystemExit(f"device status after timing: {qlin.status_string(st)} "
@@ -458,7 +471,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     ms = t_step / args.steps * 1e3
-    value = runner.weight_bytes * args.steps * world / t_step / 1e9
+    value = whole_job_rate(runner.weight_bytes, args.steps, world, t_step) / 1e9
     hbm, bf16, peak_src = measured_peaks()
     gemm_avg_s = t_gemm / (args.steps * runner.n_gemm(fused))
     bytes_per_launch = runner.gemm_bytes(fused) / runner.n_gemm(fused)
@@ -638,10 +651,16 @@ def run_producers(args, rank, world, local_rank):
     if qlin.device_status() != qlin.QLIN_OK:
         raise SystemExit("device status after warm-up is not OK")
     clocks = ClockSampler(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize()
     clocks.start()
     t_step = time_graph(torch, step_graph, args.steps)
     t_top = time_graph(torch, top_graph, args.steps)
     clock_info = clocks.stop()
+    t_step, t_top = max_over_ranks([t_step, t_top], device)
 
     host_in = [c[3].cpu().pin_memory() for c in calls]
     host_q = [torch.empty(c[5].shape, dtype=torch.int8, pin_memory=True) for c in calls]
@@ -667,6 +686,7 @@ def run_producers(args, rank, world, local_rank):
         e2e_step()
     torch.cuda.synchronize()
     t_e2e = (time.perf_counter() - t0) / reps
+    t_e2e, = max_over_ranks([t_e2e], device)
     if qlin.device_status() != qlin.QLIN_OK:
         raise SystemExit("device status after timing is not OK")
     if rank != 0:
@@ -678,7 +698,7 @@ def run_producers(args, rank, world, local_rank):
     achieved = top_bytes / top_s / 1e9
     return {
         "metric": "fused producer + INT8 act-quant GB/s (algorithmic bytes); % of HBM roofline",
-        "value": round(step_bytes * args.steps * world / t_step / 1e9, 2),
+        "value": round(whole_job_rate(step_bytes, args.steps, world, t_step) / 1e9, 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
