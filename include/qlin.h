@@ -34,7 +34,10 @@
  *  - No exception crosses the ABI and nothing is printed.
  *  - Shapes: M = tokens (rows of the activation), K = input features,
  *    N = output features.  K must be a positive multiple of 128, N a positive
- *    multiple of 8, M >= 0 (M == 0 is a no-op), and M, N, K <= 2^31 - 1.
+ *    multiple of 8, M >= 0, and M, N, K <= 2^31 - 1.  M == 0 (an empty
+ *    batch) reads and writes nothing and returns QLIN_OK after the shape
+ *    checks; the pointers sized by M (activations, their scales, outputs)
+ *    may then be NULL.
  *  - Alignment: every pointer must be 16-byte aligned (the kernels move data
  *    with TMA and 16-byte vector accesses), unless a call states otherwise.
  *  - The calls run only on an sm_103 GPU (GB300); elsewhere they return

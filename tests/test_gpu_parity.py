@@ -568,3 +568,32 @@ def test_fused_producers_reject_bad_shapes():
         qlin.rmsnorm_act_quant_i8(x, g, -1.0)                 # negative eps
     with pytest.raises(qlin.QlinError):
         qlin.silu_mul_act_quant_i8(torch.zeros((4, 200), dtype=torch.bfloat16, device="cuda"))
+
+
+def test_empty_batch_is_a_no_op_everywhere():
+    """M = 0 through every call of the binding: empty outputs, QLIN_OK, no
+    device error (the batch-sized buffers of an empty batch are NULL)."""
+    K, N = 256, 128
+    dev = "cuda"
+    x = torch.empty((0, K), dtype=torch.bfloat16, device=dev)
+    q, s = qlin.act_quant_i8(x)
+    assert q.shape == (0, K) and s.shape == (0,)
+    g = torch.ones((K,), dtype=torch.bfloat16, device=dev)
+    q, s = qlin.rmsnorm_act_quant_i8(x, g, 1e-6)
+    assert q.shape == (0, K)
+    q, s = qlin.silu_mul_act_quant_i8(torch.empty((0, 2 * K), dtype=torch.bfloat16, device=dev))
+    assert q.shape == (0, K)
+    qa = torch.empty((0, K), dtype=torch.int8, device=dev)
+    sa = torch.empty((0,), dtype=torch.float32, device=dev)
+    qw8 = torch.zeros((K // 4, N), dtype=torch.int32, device=dev)
+    qw4 = torch.zeros((K // 8, N), dtype=torch.int32, device=dev)
+    s16 = torch.ones((K // 128, N), dtype=torch.float16, device=dev)
+    sb16 = torch.ones((K // 128, N), dtype=torch.bfloat16, device=dev)
+    assert qlin.gemm_w8a8_gs128(qa, sa, qw8, s16).shape == (0, N)
+    assert qlin.gemm_w8a8_gs128_noalloc(qa, sa, qw8, s16).shape == (0, N)
+    assert qlin.gemm_w4a16_g128(x, qw4, sb16).shape == (0, N)
+    assert qlin.gemm_w8a16(x, qw8, sb16, 128).shape == (0, N)
+    assert qlin.gemm_w8a8_gs128_argmax(qa, sa, qw8, s16).shape == (0,)
+    assert qlin.gemm_w4a16_g128_argmax(x, qw4, sb16).shape == (0,)
+    torch.cuda.synchronize()
+    assert qlin.device_status() == qlin.QLIN_OK

@@ -92,10 +92,11 @@ struct Cfg {
   // 128-wide K groups per pipeline step.  W4A16 at token tiles up to 32 takes
   // two: a step then carries 16 KB of weights like the 8-bit formats, which
   // halves the fixed per-step cost (synchronisation, MMA issue) per byte.  At
-  // 64-token tiles the larger activation slots would halve the weight bytes
-  // in flight, and two-group steps measured no faster there.
+  // 64-token tiles the larger activation slots halve the weight bytes in
+  // flight, which costs more than it saves on short ranges: there two-group
+  // steps are taken only when every block gets at least 16 of them.
   static constexpr int kGPS = GPS;
-  static_assert(GPS == 1 || (GPS == 2 && kInt4 && T <= 32), "two-group steps: W4A16, T <= 32");
+  static_assert(GPS == 1 || (GPS == 2 && kInt4 && T <= 64), "two-group steps: W4A16, T <= 64");
   // warps 0..3: control (0 weight TMA, 1 TMEM owner + MMA issuer, 2 activation
   //             and scale TMA, 3 MMA issuer)
   // warps 4..11: converters, two groups of four taking alternate steps (each
@@ -1179,7 +1180,10 @@ cudaError_t launch_mode(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStr
     case 32:
       if (kMode == kModeW4 && a.K % 256 == 0) return launch_t<kMode, 32, kMode == kModeW4 ? 2 : 1>(a, pl, err, stream);
       return launch_t<kMode, 32, 1>(a, pl, err, stream);
-    case 64: return launch_t<kMode, 64, 1>(a, pl, err, stream);
+    case 64:
+      if (kMode == kModeW4 && a.K % 256 == 0 && pl.TT * pl.F * (pl.G / 2) >= 16 * pl.ctas)
+        return launch_t<kMode, 64, kMode == kModeW4 ? 2 : 1>(a, pl, err, stream);
+      return launch_t<kMode, 64, 1>(a, pl, err, stream);
     case 96: return launch_t<kMode, 96, 1>(a, pl, err, stream);
     default: return launch_t<kMode, 128, 1>(a, pl, err, stream);
   }

@@ -62,7 +62,8 @@ extern "C" qlin_status_t qlin_gemm_w8a8_gs128_noalloc(const int8_t* q_a, const f
                                                       const uint16_t* scales, int64_t M,
                                                       int64_t N, int64_t K, uint16_t* y,
                                                       qlin_stream_t stream) {
-  if (q_a == nullptr || s_a == nullptr || qweight == nullptr || scales == nullptr || y == nullptr)
+  if ((M != 0 && (q_a == nullptr || s_a == nullptr || y == nullptr)) || qweight == nullptr ||
+      scales == nullptr)
     return QLIN_ERR_NULL;
   if (M < 0 || M > 2147483647LL || N < 8 || N > 2147483647LL || (N % 8) != 0 || K < kGroup ||
       K > 2147483647LL || (K % kGroup) != 0)

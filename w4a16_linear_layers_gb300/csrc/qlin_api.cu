@@ -82,9 +82,11 @@ qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const i
                        const uint16_t* scales, void* out, int64_t M, int64_t N, int64_t K,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream,
                        int group_size = 128) {
-  if (act == nullptr || qweight == nullptr || out == nullptr ||
-      (mode != GemmMode::kW8A8Partials && scales == nullptr) ||
-      (mode == GemmMode::kW8A8 && s_a == nullptr))
+  // an empty batch reads and writes nothing: its activation, scale and
+  // output pointers may be NULL
+  const bool rows = M != 0;
+  if ((rows && (act == nullptr || out == nullptr || (mode == GemmMode::kW8A8 && s_a == nullptr))) ||
+      qweight == nullptr || (mode != GemmMode::kW8A8Partials && scales == nullptr))
     return QLIN_ERR_NULL;
   qlin_status_t st = check_gemm_shape(M, N, K);
   if (st != QLIN_OK) return st;
@@ -108,8 +110,9 @@ qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const i
 qlin_status_t run_argmax(GemmMode mode, const void* act, const float* s_a, const int32_t* qweight,
                          const uint16_t* scales, int32_t* idx, int64_t M, int64_t N, int64_t K,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (act == nullptr || qweight == nullptr || scales == nullptr || idx == nullptr ||
-      (mode == GemmMode::kW8A8 && s_a == nullptr))
+  const bool rows = M != 0;
+  if ((rows && (act == nullptr || idx == nullptr || (mode == GemmMode::kW8A8 && s_a == nullptr))) ||
+      qweight == nullptr || scales == nullptr)
     return QLIN_ERR_NULL;
   qlin_status_t st = check_gemm_shape(M, N, K);
   if (st != QLIN_OK) return st;
@@ -142,7 +145,7 @@ extern "C" {
 
 qlin_status_t qlin_act_quant_i8(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s_a,
                                 qlin_stream_t stream) {
-  if (x == nullptr || q == nullptr || s_a == nullptr) return QLIN_ERR_NULL;
+  if (M != 0 && (x == nullptr || q == nullptr || s_a == nullptr)) return QLIN_ERR_NULL;
   if (M < 0 || M > kMaxDim || K < kGroup || K > kMaxDim || (K % kGroup) != 0)
     return QLIN_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(q) || !aligned16(s_a)) return QLIN_ERR_ALIGN;
@@ -156,7 +159,8 @@ qlin_status_t qlin_act_quant_i8(const uint16_t* x, int64_t M, int64_t K, int8_t*
 qlin_status_t qlin_rmsnorm_act_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps,
                                         int64_t M, int64_t K, int8_t* q, float* s_a, uint16_t* y,
                                         qlin_stream_t stream) {
-  if (x == nullptr || gamma == nullptr || q == nullptr || s_a == nullptr) return QLIN_ERR_NULL;
+  if (gamma == nullptr || (M != 0 && (x == nullptr || q == nullptr || s_a == nullptr)))
+    return QLIN_ERR_NULL;
   if (M < 0 || M > kMaxDim || K < kGroup || K > kMaxDim || (K % kGroup) != 0 || !(eps >= 0.0f) ||
       !std::isfinite(eps))
     return QLIN_ERR_SHAPE;
@@ -173,7 +177,7 @@ qlin_status_t qlin_rmsnorm_act_quant_i8(const uint16_t* x, const uint16_t* gamma
 
 qlin_status_t qlin_silu_mul_act_quant_i8(const uint16_t* gate_up, int64_t M, int64_t I, int8_t* q,
                                          float* s_a, uint16_t* y, qlin_stream_t stream) {
-  if (gate_up == nullptr || q == nullptr || s_a == nullptr) return QLIN_ERR_NULL;
+  if (M != 0 && (gate_up == nullptr || q == nullptr || s_a == nullptr)) return QLIN_ERR_NULL;
   if (M < 0 || M > kMaxDim || I < kGroup || I > kMaxDim || (I % kGroup) != 0)
     return QLIN_ERR_SHAPE;
   if (!aligned16(gate_up) || !aligned16(q) || !aligned16(s_a) || (y != nullptr && !aligned16(y)))
