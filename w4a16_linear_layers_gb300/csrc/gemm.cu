@@ -492,7 +492,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int first_w = w_issued;
       for (int j = w_issued; j < n_steps; ++j, it.next(), rg.next()) {
-        if (j == first_w && !mbar_wait(smem_u32(&ctrl->x_go), 0u, ctx, 19)) break;
+        // The weight-only formats read bf16 activations that are usually
+        // ready at launch, so their first tiles go ahead of the weight ring
+        // (x_go).  W8A8 activations come from the act-quant kernel launched
+        // just before: the weights fill the ring while it runs.
+        if (C::kWO && j == first_w && !mbar_wait(smem_u32(&ctrl->x_go), 0u, ctx, 19)) break;
         if (!mbar_wait(smem_u32(&ctrl->empty[rg.slot]), rg.phase ^ 1u, ctx, 1)) break;
         const uint32_t full = smem_u32(&ctrl->wfull[rg.slot]);
         mbar_arrive_expect_tx(full, C::kWBytes);
