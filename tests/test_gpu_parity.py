@@ -40,6 +40,7 @@ def _act_quant_gpu(xb):
 @pytest.mark.parametrize("M,K,kind", [
     (1, 128, "normal"), (3, 5120, "outliers"), (8, 5120, "outliers"), (17, 4096, "normal2"),
     (96, 17408, "silu_mul"), (5, 25600, "normal2"), (4, 33024, "outliers"), (130, 640, "normal"),
+    (300, 1280, "outliers"), (260, 40960, "normal"),   # more than 256 rows: 256-thread blocks
 ])
 def test_act_quant_bit_exact(M, K, kind):
     xb = synth.activations(1, f"gpu/aq/{M}/{K}", M, K, kind)

@@ -5,9 +5,10 @@
 // "Qwen3.8-27B-GPTQ-INT8-W8A8-GS128-PTQR" card, "Serving" (GEMM inputs are
 // dynamically quantized to INT8).
 //
-// One block of 256 threads per row.  The row is read once with 16-byte
-// vector loads and kept in registers (rows of up to 32768 elements; longer
-// rows are read twice, the second time from L2); the row maximum of |x| is
+// One block per row (1024 threads for up to 256 rows, else 256).  The row is
+// read once with 16-byte vector loads and kept in registers (rows of up to
+// 32768 elements; longer rows are read twice, the second time from L2); the
+// row maximum of |x| is
 // reduced with warp shuffles and one shared-memory step; then
 // s = amax / 127 and q = rint(x / s) are formed with IEEE fp32 division
 // (div.rn), exactly as the format defines them, and written as 8-byte stores.
@@ -21,8 +22,8 @@
 namespace qlin {
 namespace {
 
-constexpr int kAqThreads = 256;
-constexpr int kAqVecPerThread = 16;  // 16 x 8 bf16 = 128 elements per thread in registers
+constexpr int kAqThreads = 256;        // the long-row producer kernels
+constexpr int kAqRowVecs = 4096;       // rows of up to 4096 x 8 elements stay in registers
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -77,11 +78,14 @@ __device__ __forceinline__ uint2 quant8y(uint4 v, float s, float y) {
   return o;
 }
 
-template <bool kCached>
-__global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint16_t* __restrict__ x,
-                                                               int64_t K, int8_t* __restrict__ q,
-                                                               float* __restrict__ s_out) {
-  __shared__ float red[kAqThreads / 32];
+// kThreads threads per row: 1024 for small batches (each row's latency is the
+// whole call's), 256 for many rows (several blocks per SM).
+template <bool kCached, int kThreads>
+__global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __restrict__ x,
+                                                             int64_t K, int8_t* __restrict__ q,
+                                                             float* __restrict__ s_out) {
+  constexpr int kVec = kAqRowVecs / kThreads;
+  __shared__ float red[kThreads / 32];
   // Launched with programmatic serialization: wait for the previous kernel
   // (which may produce x or still read q) before touching memory, then let
   // the next kernel (a GEMM that streams weights first) start.
@@ -93,19 +97,19 @@ __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint16_t* _
   uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
   const int tid = threadIdx.x;
 
-  uint4 cache[kCached ? kAqVecPerThread : 1];
+  uint4 cache[kCached ? kVec : 1];
   float amax = 0.0f;
   if (kCached) {
 #pragma unroll
-    for (int i = 0; i < kAqVecPerThread; ++i) {
-      const int64_t v = tid + static_cast<int64_t>(i) * kAqThreads;
+    for (int i = 0; i < kVec; ++i) {
+      const int64_t v = tid + static_cast<int64_t>(i) * kThreads;
       if (v < nvec) {
         cache[i] = __ldg(row + v);
         amax = absmax8(cache[i], amax);
       }
     }
   } else {
-    for (int64_t v = tid; v < nvec; v += kAqThreads) amax = absmax8(__ldg(row + v), amax);
+    for (int64_t v = tid; v < nvec; v += kThreads) amax = absmax8(__ldg(row + v), amax);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
@@ -113,23 +117,23 @@ __global__ void __launch_bounds__(kAqThreads) act_quant_kernel(const uint16_t* _
   __syncthreads();
   amax = red[0];
 #pragma unroll
-  for (int w = 1; w < kAqThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+  for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, red[w]);
 
   const float s = __fdiv_rn(amax, 127.0f);
   if (tid == 0) s_out[m] = s;
   if (amax == 0.0f) {
-    for (int64_t v = tid; v < nvec; v += kAqThreads) qrow[v] = make_uint2(0u, 0u);
+    for (int64_t v = tid; v < nvec; v += kThreads) qrow[v] = make_uint2(0u, 0u);
     return;
   }
   const float y = __frcp_rn(s);
   if (kCached) {
 #pragma unroll
-    for (int i = 0; i < kAqVecPerThread; ++i) {
-      const int64_t v = tid + static_cast<int64_t>(i) * kAqThreads;
+    for (int i = 0; i < kVec; ++i) {
+      const int64_t v = tid + static_cast<int64_t>(i) * kThreads;
       if (v < nvec) qrow[v] = quant8y(cache[i], s, y);
     }
   } else {
-    for (int64_t v = tid; v < nvec; v += kAqThreads) qrow[v] = quant8y(__ldg(row + v), s, y);
+    for (int64_t v = tid; v < nvec; v += kThreads) qrow[v] = quant8y(__ldg(row + v), s, y);
   }
 }
 
@@ -509,9 +513,12 @@ cudaError_t launch_silu_mul_quant(const uint16_t* gate_up, int64_t M, int64_t I,
 cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s,
                              cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(M));
-  if (K <= static_cast<int64_t>(kAqThreads) * kAqVecPerThread * 8)
-    return launch_pdl(act_quant_kernel<true>, grid, dim3(kAqThreads), 0, stream, x, K, q, s);
-  return launch_pdl(act_quant_kernel<false>, grid, dim3(kAqThreads), 0, stream, x, K, q, s);
+  const bool cached = K <= static_cast<int64_t>(kAqRowVecs) * 8;
+  if (M <= 256)
+    return cached ? launch_pdl(act_quant_kernel<true, 1024>, grid, dim3(1024), 0, stream, x, K, q, s)
+                  : launch_pdl(act_quant_kernel<false, 1024>, grid, dim3(1024), 0, stream, x, K, q, s);
+  return cached ? launch_pdl(act_quant_kernel<true, 256>, grid, dim3(256), 0, stream, x, K, q, s)
+                : launch_pdl(act_quant_kernel<false, 256>, grid, dim3(256), 0, stream, x, K, q, s);
 }
 
 }  // namespace qlin
