@@ -773,10 +773,11 @@ def run_producers(args, rank, world, local_rank):
     }
 
 
-def producer_oracle_sample(budget_s, seed=0):
-    """The oracle on the whole step (every row of every call), repeated while
-    the time stays under half the budget, on all host cores (one thread per
-    row slice).  Returns (algorithmic bytes covered, seconds, threads, text)."""
+def producer_oracle_sample(budget_s, seed=0, rows=None):
+    """The oracle on the first `rows` rows of every call of the step (the
+    whole step when rows is None), repeated while the time stays under half
+    the budget, on all host cores (one thread per row slice).
+    Returns (algorithmic bytes covered, seconds, threads, text)."""
     from concurrent.futures import ThreadPoolExecutor
 
     import oracle
@@ -787,8 +788,9 @@ def producer_oracle_sample(budget_s, seed=0):
     tasks, step_bytes = [], 0
     for kind, M, K in specs:
         x, g = producer_inputs(kind, M, K, seed)
-        step_bytes += producer_bytes(kind, M, K)
-        for sl in np.array_split(np.arange(M), min(nthreads, M)):
+        r = M if rows is None else min(rows, M)
+        step_bytes += producer_bytes(kind, r, K)
+        for sl in np.array_split(np.arange(r), min(nthreads, r)):
             if sl.size:
                 tasks.append((kind, np.ascontiguousarray(x[sl]), g))
 
@@ -805,8 +807,9 @@ def producer_oracle_sample(budget_s, seed=0):
             list(ex.map(lambda t: work(*t), tasks))
         total += time.perf_counter() - t0
         reps += 1
+    what = "every row" if rows is None else f"the first {rows} rows"
     return step_bytes * reps, total, nthreads, (
-        f"oracle on the whole step ({len(specs)} calls, every row), {reps} time(s), "
+        f"oracle on {what} of each of the {len(specs)} calls of the step, {reps} time(s), "
         f"{nthreads} threads")
 
 
@@ -819,11 +822,12 @@ def cores():
         return os.cpu_count() or 1
 
 
-def oracle_sample(specs, budget_s, seed=0, cache=None):
+def oracle_sample(specs, budget_s, seed=0, cache=None, frac=None):
     """Time the oracle on a bounded sample of the workload: for every linear
     of the step, the same fraction of its output columns (all rows), run on
     all host cores (one thread per column slice; the C oracle runs without the
-    GIL).  Returns (weight bytes covered, seconds, threads, description)."""
+    GIL).  The fraction is calibrated to the time budget unless given.
+    Returns (weight bytes covered, seconds, threads, description, fraction)."""
     from concurrent.futures import ThreadPoolExecutor
 
     import oracle
@@ -861,7 +865,10 @@ def oracle_sample(specs, budget_s, seed=0, cache=None):
         for name, K, N, kind, M, wk in specs:
             nc = max(1, int(round(N * frac)))
             total_bytes += weight_bytes(K, nc, wk)
-            fn = operands(name, K, N, kind, M, wk, nc)
+            key = ("operands", name, K, N, kind, M, wk, nc)
+            if key not in cache:
+                cache[key] = operands(name, K, N, kind, M, wk, nc)
+            fn = cache[key]
             for ch in np.array_split(np.arange(nc), min(nthreads, nc)):
                 if ch.size:
                     tasks.append((fn, ch))
@@ -870,25 +877,35 @@ def oracle_sample(specs, budget_s, seed=0, cache=None):
             list(ex.map(lambda t: t[0](t[1]), tasks))
         return total_bytes, time.perf_counter() - t0
 
-    frac = 0.001
-    while True:                       # calibrate the sample size on this host
-        _, t = run(frac)
-        if t >= 0.2 * budget_s or frac >= 1.0:
-            break
-        frac = min(1.0, frac * min(16.0, max(2.0, 0.3 * budget_s / max(t, 1e-3))))
-    frac = min(1.0, frac * budget_s / max(t, 1e-3))
+    if frac is None:
+        frac = 0.001
+        while True:                       # calibrate the sample size on this host
+            _, t = run(frac)
+            if t >= 0.2 * budget_s or frac >= 1.0:
+                break
+            frac = min(1.0, frac * min(16.0, max(2.0, 0.3 * budget_s / max(t, 1e-3))))
+        frac = min(1.0, frac * budget_s / max(t, 1e-3))
     b, t = run(frac)
     desc = (f"oracle on {frac * 100:.3f}% of the output columns of every linear of the step "
             f"(all rows), {nthreads} threads")
-    return b, t, nthreads, desc
+    return b, t, nthreads, desc, frac
 
 
 def run_reference_producers(args):
+    # about a minute of oracle work over all steps: rows per call calibrated
+    # once so that one step takes the per-step budget
+    budget = max(0.02, 60.0 / max(1, args.steps + args.warmup))
+    rows = 1
+    while rows < 8192:
+        _, t, _, _ = producer_oracle_sample(0.0, rows=rows)
+        if t >= budget:
+            break
+        rows *= 2
     for _ in range(args.warmup):
-        producer_oracle_sample(1.0)
+        producer_oracle_sample(0.0, rows=rows)
     tot_b, tot_t, thr, desc = 0, 0.0, 1, ""
     for _ in range(args.steps):
-        b, t, thr, desc = producer_oracle_sample(max(1.0, 30.0 / max(1, args.steps)))
+        b, t, thr, desc = producer_oracle_sample(0.0, rows=rows)
         tot_b += b
         tot_t += t
     value = tot_b / tot_t / 1e9
@@ -914,14 +931,17 @@ def run_reference(args, rank, world):
     if args.workload == "producers":
         return run_reference_producers(args)
     specs = workload_specs(args.workload)
-    per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    # about a minute of oracle work over all warm-up and timed steps: the
+    # sample fraction is calibrated once, then every step runs that sample
+    per_step_budget = max(0.02, 60.0 / max(1, args.steps + args.warmup))
     cache = {}
+    _, _, _, _, frac = oracle_sample(specs, per_step_budget, cache=cache)
     for _ in range(args.warmup):
-        oracle_sample(specs, min(per_step_budget, 2.0), cache=cache)
+        oracle_sample(specs, per_step_budget, cache=cache, frac=frac)
     tot_b, tot_t = 0, 0.0
     desc, thr = "", 1
     for _ in range(args.steps):
-        b, t, thr, desc = oracle_sample(specs, per_step_budget, cache=cache)
+        b, t, thr, desc, _ = oracle_sample(specs, per_step_budget, cache=cache, frac=frac)
         tot_b += b
         tot_t += t
     value = tot_b / tot_t / 1e9
@@ -992,7 +1012,7 @@ def main():
         out = run_ours(args, rank, world, local_rank)
     if out is not None:
         line, runner = out
-        b, t, thr, desc = oracle_sample(runner.specs, args.cpu_budget)
+        b, t, thr, desc, _ = oracle_sample(runner.specs, args.cpu_budget)
         line["cpu_baseline"] = {"value": round(b / t / 1e9, 6), "unit": "GB/s", "cores": thr,
                                 "kind": "oracle", "sample": desc}
         print(json.dumps(line), flush=True)
