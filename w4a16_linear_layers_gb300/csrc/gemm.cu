@@ -1203,7 +1203,10 @@ cudaError_t launch_argmax_finalize(const unsigned long long* keys, int64_t M, in
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
   GemmPlan p{};
-  p.T = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 96 ? 96 : 128;
+  // 96-token tiles also for large batches: at M = 2048 and 8192 they ran the
+  // W8A8 MLP projections 3-12% faster than 128-token tiles (more D buffers
+  // per group for the per-group rescale), ragged last tile included
+  p.T = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 96 ? 96 : M >= 1024 ? 96 : 128;
   p.F = (N + kTileF - 1) / kTileF;
   p.TT = (M + p.T - 1) / p.T;
   p.G = K / kGroup;
