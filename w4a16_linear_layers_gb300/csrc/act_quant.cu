@@ -1,17 +1,20 @@
-// act_quant.cu -- dynamic per-token symmetric INT8 activation quantization.
+// act_quant.cu -- dynamic per-token symmetric INT8 activation quantization,
+// alone and fused into the producers of the projections' inputs.
 //
 // Passages: "Flint-DFlash2-GPTQ-INT8-PTQR" model card (dynamic per-token
-// activation quantization; VLLM_GFX908_ACT_QUANT=round) and
+// activation quantization; VLLM_GFX908_ACT_QUANT=round);
 // "Qwen3.8-27B-GPTQ-INT8-W8A8-GS128-PTQR" card, "Serving" (GEMM inputs are
-// dynamically quantized to INT8).
+// dynamically quantized to INT8); "Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ"
+// card (the BF16 norms in front of the q/k/v and gate/up projections, the
+// gated MLP in front of down_proj).
 //
-// One block per row (1024 threads for up to 256 rows, else 256).  The row is
-// read once with 16-byte vector loads and kept in registers (rows of up to
-// 32768 elements; longer rows are read twice, the second time from L2); the
-// row maximum of |x| is
-// reduced with warp shuffles and one shared-memory step; then
-// s = amax / 127 and q = rint(x / s) are formed with IEEE fp32 division
-// (div.rn), exactly as the format defines them, and written as 8-byte stores.
+// act_quant_kernel: one block per row (1024 threads for up to 256 rows, else
+// 256).  The row is read once with 16-byte vector loads and kept in registers
+// (rows of up to 32768 elements; longer rows are read twice, the second time
+// from L2).  The row maximum of |x| is reduced with warp shuffles and one
+// shared-memory step; s = amax / 127 is an IEEE fp32 divide, and the codes are
+// those of rint(x / s) with an IEEE divide (quant1y), written as 8-byte
+// stores.  The producer kernels are described at "fused producers" below.
 #include <cuda_bf16.h>
 
 #include <mutex>
