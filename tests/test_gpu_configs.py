@@ -47,14 +47,21 @@ def sample_rows(M, seed, limit=96):
     return np.concatenate([[0], rows + 1, [M - 1]])
 
 
-def run_w8a8(name, M, K, N, kind, seed=0):
+def run_w8a8(name, M, K, N, kind, seed=0, argmax=False):
     xb = synth.activations(seed, synth.shared_input_name(name) + f"/M{M}", M, K, kind)
     qwt, swb = synth.w8a8_weights(seed, name, K, N)
     qw, _, _ = oracle.pack_gptq(qwt, 8)
     del qwt
     x_d = to_dev_bits(xb, torch.bfloat16)
     qa_d, sa_d = qlin.act_quant_i8(x_d)
-    y_d = qlin.gemm_w8a8_gs128(qa_d, sa_d, to_dev(qw), to_dev_bits(swb, torch.float16))
+    qw_d, sw_d = to_dev(qw), to_dev_bits(swb, torch.float16)
+    y_d = qlin.gemm_w8a8_gs128(qa_d, sa_d, qw_d, sw_d)
+    if argmax:
+        # the fused greedy argmax must pick, per row, the first maximum of the
+        # very outputs the plain call wrote
+        idx = qlin.gemm_w8a8_gs128_argmax(qa_d, sa_d, qw_d, sw_d)
+        want = y_d.float().argmax(dim=1).to(torch.int32)
+        assert torch.equal(idx, want), f"{name} M={M}: fused argmax differs"
     torch.cuda.synchronize()
     qa, sa = oracle.act_quant_i8(xb)
     assert np.array_equal(qa_d.cpu().numpy(), qa) and np.array_equal(sa_d.cpu().numpy(), sa)
@@ -109,4 +116,47 @@ def test_prefill_mlp_w8a8(M):
 
 @pytest.mark.parametrize("M", [8, 96])
 def test_vocab_head_w8a8(M):
-    run_w8a8("lm_head", M, 5120, 248320, "outliers")
+    run_w8a8("lm_head", M, 5120, 248320, "outliers", argmax=True)
+
+
+@pytest.mark.parametrize("M", [8, 64, 96])
+def test_fused_gate_up_full_size_w8a8(M):
+    """gate_proj and up_proj as one GEMM over their weights concatenated along
+    N (5120 -> 2 x 17408), as the benchmark runs them: sampled columns of each
+    half against the oracle of its own projection."""
+    K, I = 5120, 17408
+    xb = synth.activations(0, f"layers.0.gate_proj/M{M}", M, K, "outliers")
+    qa, sa = oracle.act_quant_i8(xb)
+    parts = [synth.w8a8_weights(0, f"layers.0.{n}", K, I) for n in ("gate_proj", "up_proj")]
+    packed = [oracle.pack_gptq(q, 8)[0] for q, _ in parts]
+    qw_cat = np.ascontiguousarray(np.concatenate(packed, axis=1))
+    sw_cat = np.ascontiguousarray(np.concatenate([s for _, s in parts], axis=1))
+    y_d = qlin.gemm_w8a8_gs128(to_dev(qa), to_dev(sa), to_dev(qw_cat),
+                               to_dev_bits(sw_cat, torch.float16))
+    torch.cuda.synchronize()
+    y = from_dev_bits(y_d)
+    rows = sample_rows(M, 0)
+    for half, (qw, (_, sw)) in enumerate(zip(packed, parts)):
+        cols = sample_cols(I, half)
+        ref = oracle.gemm_w8a8_gs128(qa, sa, qw, sw, K, rows, cols)
+        compare_linear(y[np.ix_(rows, cols + half * I)], ref, f"gate_up half {half} M={M}")
+
+
+def run_w8a16(name, M, K, N, seed=0, gs=32):
+    xb = synth.activations(seed, synth.shared_input_name(name) + f"/w8a16/M{M}", M, K, "normal")
+    qwt, sb = synth.w8a16_weights(seed, name + "/w8a16", K, N, gs)
+    qw, _, _ = oracle.pack_gptq(qwt, 8)
+    del qwt
+    y_d = qlin.gemm_w8a16(to_dev_bits(xb, torch.bfloat16), to_dev(qw),
+                          to_dev_bits(sb, torch.bfloat16), gs)
+    torch.cuda.synchronize()
+    rows, cols = sample_rows(M, seed), sample_cols(N, seed)
+    y = from_dev_bits(y_d)[np.ix_(rows, cols)]
+    ref = oracle.gemm_w8a16(xb, qw, sb, K, gs, rows, cols)
+    return compare_linear(y, ref, f"{name} w8a16 M={M}")
+
+
+@pytest.mark.parametrize("M", [8, 64])
+def test_drafter_layer_w8a16_group32(M):
+    for name, K, N, _ in synth.DRAFTER_LAYER:
+        run_w8a16(f"layers.0.{name}", M, K, N)
