@@ -359,7 +359,11 @@ qlin_status_t qlin_device_error_detail(qlin_stream_t stream, int32_t *where, int
 /* A static, human-readable name for a status code. */
 const char *qlin_status_string(qlin_status_t status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor).  1.1 (101) adds the W8A16
+ * GEMM, the greedy-argmax GEMMs, the compressed-tensors ingest, the fused
+ * producers and qlin_device_error_detail to the 1.0 calls; no 1.0 call
+ * changed, except that an empty batch (M == 0) now accepts NULL batch
+ * buffers. */
 int qlin_version(void);
 
 #ifdef __cplusplus

@@ -338,6 +338,6 @@ const char* qlin_status_string(qlin_status_t status) {
   }
 }
 
-int qlin_version(void) { return 100; }
+int qlin_version(void) { return 101; }
 
 }  // extern "C"
