@@ -170,6 +170,29 @@ def test_w8a8_matches_oracle(M, K, N):
     compare_linear(y, oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K), f"w8a8 {M}x{K}x{N}")
 
 
+def test_w8a8_extreme_fp16_scales():
+    """Weight scales over the whole positive fp16 range, subnormals to 65504,
+    mixed per group and column: the fp32 rescale chain must still match."""
+    M, K, N = 8, 1024, 384
+    _, qa, sa, _, qw, _ = _w8a8_inputs(21, "gpu/w8/extreme", M, K, N)
+    rng = np.random.default_rng(21)
+    exps = rng.uniform(-24.0, 15.9, size=(K // 128, N))
+    scales = np.clip(np.exp2(exps), 2.0 ** -24, 65504.0)
+    swb = synth.f16_bits(scales)
+    y = _gemm_w8a8_gpu(qa, sa, qw, swb)
+    compare_linear(y, oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K), "w8a8 extreme scales")
+
+
+def test_w4a16_wide_range_bf16_scales():
+    """bf16 weight scales from 2^-30 to 2^30, mixed per group and column."""
+    M, K, N = 8, 1024, 384
+    xb, _, qw, _ = _w4a16_inputs(22, "gpu/w4/wide", M, K, N)
+    rng = np.random.default_rng(22)
+    sb = synth.bf16_bits(np.exp2(rng.uniform(-30.0, 30.0, size=(K // 128, N))))
+    y = _gemm_w4a16_gpu(xb, qw, sb)
+    compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), "w4a16 wide scales")
+
+
 def test_w8a8_identity_probe():
     """Feeding I_K recovers the effective weight q*s (single nonzero group per
     row, so every split of K gives the oracle's exact fp32 chain)."""
