@@ -584,3 +584,49 @@ def test_fused_producers_compose_with_act_quant(oracle_lib):
     q, s, z = oracle_lib.silu_mul_act_quant_i8(gu)
     q2, s2 = oracle_lib.act_quant_i8(z)
     assert np.array_equal(q, q2) and np.array_equal(s, s2) and z.shape == (5, 384)
+
+
+# ------------------------------------------------------------ equivariance
+
+def test_act_quant_power_of_two_and_sign_equivariance(oracle_lib):
+    """Scaling a row by 2^j scales s by 2^j and keeps q (every step is exact
+    under a power of two); negating a row negates q and keeps s."""
+    xb = synth.activations(5, "pin/eqv", 12, 640, "outliers")
+    q, s = oracle_lib.act_quant_i8(xb)
+    x = synth.bf16_values(xb)
+    for j in (-9, 4, 30):
+        q2, s2 = oracle_lib.act_quant_i8(bf16_of(x * np.float32(2.0 ** j)))
+        assert np.array_equal(q2, q)
+        assert np.array_equal(s2, (s * np.float32(2.0 ** j)).astype(np.float32))
+    qn, sn = oracle_lib.act_quant_i8(xb ^ np.uint16(0x8000))
+    assert np.array_equal(qn, -q) and np.array_equal(sn, s)
+
+
+def test_w8a8_scale_and_sign_equivariance(oracle_lib):
+    """Doubling every weight scale doubles the fp32 chain exactly; negating
+    every weight negates it exactly (round-to-nearest is symmetric)."""
+    M, K, N = 5, 768, 96
+    xb = synth.activations(6, "pin/eqv8/x", M, K, "normal")
+    qa, sa = oracle_lib.act_quant_i8(xb)
+    qwt, swb = synth.w8a8_weights(6, "pin/eqv8/w", K, N)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 8)
+    base = oracle_lib.gemm_w8a8_gs128(qa, sa, qw, swb, K)
+    sw2 = synth.f16_bits(swb.view(np.float16).astype(np.float64) * 2.0)
+    dbl = oracle_lib.gemm_w8a8_gs128(qa, sa, qw, sw2, K)
+    assert np.array_equal(dbl["y_f32"], base["y_f32"] * np.float32(2.0))
+    qwn, _, _ = oracle_lib.pack_gptq((-qwt.astype(np.int16)).astype(np.int8), 8)
+    neg = oracle_lib.gemm_w8a8_gs128(qa, sa, qwn, swb, K)
+    assert np.array_equal(neg["y_f32"], -base["y_f32"])
+
+
+def test_w4a16_scale_equivariance(oracle_lib):
+    """Doubling every bf16 scale doubles each dequantized weight exactly, and
+    so the fp32 accumulation."""
+    M, K, N = 4, 512, 72
+    xb = synth.activations(7, "pin/eqv4/x", M, K, "normal")
+    qwt, sb = synth.w4a16_weights(7, "pin/eqv4/w", K, N)
+    qw, _, _ = oracle_lib.pack_gptq(qwt, 4)
+    base = oracle_lib.gemm_w4a16_g128(xb, qw, sb, K)
+    sb2 = bf16_of(synth.bf16_values(sb) * np.float32(2.0))
+    dbl = oracle_lib.gemm_w4a16_g128(xb, qw, sb2, K)
+    assert np.array_equal(dbl["y_f32"], base["y_f32"] * np.float32(2.0))
