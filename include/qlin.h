@@ -314,9 +314,11 @@ qlin_status_t qlin_ingest_nk(const int32_t *packed_nk, const uint16_t *scales_ng
                              qlin_stream_t stream);
 
 /*
- * Bytes of workspace the two GEMMs need for (M, N, K) on the current device
- * (split-K partials plus one counter per output tile).  Returns 0 for shapes
- * the GEMMs reject.
+ * Bytes of workspace the GEMMs need for (M, N, K) on the current device: a
+ * fixed region of arrival counters (one per block), the fp32 split-K
+ * partials of two output tiles per block, and, for token tiles of 96 and
+ * more (M > 64), the fp16 image of the W8A8 activations.  Returns 0 for
+ * shapes the GEMMs reject.
  */
 size_t qlin_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
