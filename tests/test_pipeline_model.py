@@ -1,0 +1,83 @@
+"""Randomized checks of the GEMM kernel's mbarrier protocol (CPU only).
+
+`pipeline_model` restates each role's waits and arrivals; these tests run
+one block of every pipeline configuration the kernel builds, under random
+interleavings and random completion orders, and look for deadlocks and for
+buffers overwritten while in use.  The configurations are those of the
+kernel's configuration table: A buffers NB, accumulators ND, weight stages,
+and token slots, per format and token tile."""
+import pytest
+
+import pipeline_model as pm
+
+# (format, token tile, groups per step): the counts the kernel's configuration
+# derives from the 512 TMEM columns and 227 KB of shared memory
+CONFIGS = {
+    "W4A16 T16 two-group": dict(mode="wo", NB=2, ND=2, stages=8, NX=8),
+    "W4A16 T32 two-group": dict(mode="wo", NB=2, ND=2, stages=8, NX=4),
+    "W4A16 T64 two-group": dict(mode="wo", NB=2, ND=2, stages=4, NX=4),
+    "W4A16 T16": dict(mode="wo", NB=6, ND=2, stages=16, NX=16),
+    "W4A16 T64": dict(mode="wo", NB=4, ND=2, stages=16, NX=4),
+    "W4A16 T96": dict(mode="wo", NB=2, ND=2, stages=14, NX=4),
+    "W4A16 T128": dict(mode="wo", NB=4, ND=1, stages=10, NX=4),
+    "W8A16 T16": dict(mode="wo", NB=6, ND=2, stages=7, NX=16),
+    "W8A8 T16": dict(mode="w8x", NB=4, ND=16, stages=10, NX=4, NXR=16),
+    "W8A8 T32": dict(mode="w8x", NB=4, ND=8, stages=9, NX=4, NXR=8),
+    "W8A8 T64": dict(mode="w8x", NB=4, ND=4, stages=7, NX=4, NXR=4),
+    "W8A8 T96": dict(mode="w8", NB=2, ND=4, stages=7, NX=4),
+    "W8A8 T128": dict(mode="w8", NB=2, ND=2, stages=5, NX=4),
+}
+
+# (first step, end step, steps per tile): split tiles at both ends, whole
+# tiles in between, short segments, chunks cut by segment ends
+RANGES = [(6, 24, 20), (0, 40, 20), (19, 45, 20), (5, 60, 40), (2, 30, 8), (1, 33, 3),
+          (0, 30, 2), (130, 170, 136), (7, 8, 20)]
+ONE_GROUP = [(3, 11, 1), (0, 9, 1), (0, 24, 1), (5, 40, 1)]
+
+
+def failures(cfg, ranges, seeds):
+    out = {}
+    for s0, s1, G in ranges:
+        for seed in range(seeds):
+            r = pm.run(cfg, s0, s1, G, seed)
+            if r:
+                out.setdefault((s0, s1, G), (seed, r))
+                break
+    return out
+
+
+@pytest.mark.parametrize("name", sorted(CONFIGS))
+def test_configurations_have_no_deadlock_or_hazard(name):
+    cfg = CONFIGS[name]
+    ranges = RANGES + (ONE_GROUP if cfg["mode"] != "wo" or cfg["NB"] == 2 else [])
+    assert failures(cfg, ranges, 25) == {}
+
+
+def test_an_odd_a_buffer_count_breaks_the_protocol():
+    """With three A buffers consecutive uses of a buffer alternate between
+    the two converter groups.  A group then waits on `a_empty` for the use
+    before its own previous one, and a parity wait cannot tell "one phase
+    done" from "two phases behind": it passes early and overwrites an A
+    buffer an MMA still reads.  The kernel keeps the count even."""
+    cfg = dict(mode="wo", NB=3, ND=2, stages=8, NX=8)
+    assert failures(cfg, [(6, 24, 20), (0, 40, 20)], 60) != {}
+
+
+@pytest.mark.xfail(strict=True, reason="open: weight-only tiles of one K group with more than "
+                                       "two A buffers (K = 128, or K = 256 with one group a step)")
+@pytest.mark.parametrize("name", ["W4A16 T16", "W4A16 T64", "W8A16 T16"])
+def test_one_group_tiles_weight_only(name):
+    """Tiles of one 128-wide group make every scale chunk one step long.  A
+    converter warp releases a chunk it had no step in without waiting for it,
+    so a group running four chunks ahead adds its releases to an earlier
+    chunk's phase: the scale slot is reloaded under a warp that still reads it
+    (or the pipeline stops).  Shapes with K = 128 hit it."""
+    assert failures(CONFIGS[name], ONE_GROUP, 60) == {}
+
+
+@pytest.mark.parametrize("name", ["W4A16 T16", "W4A16 T64", "W8A16 T16"])
+def test_waiting_for_a_chunk_before_releasing_it_fixes_one_group_tiles(name):
+    """The fix for the case above: a warp that had no step in a chunk waits
+    for the chunk to land before it releases it."""
+    cfg = dict(CONFIGS[name], release_after_landing=True)
+    assert failures(cfg, ONE_GROUP + RANGES[:3], 40) == {}
