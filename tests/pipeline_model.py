@@ -19,7 +19,8 @@ The checker reports
 - a deadlock: no role can run and nothing is in flight;
 - a hazard: a buffer written while a reader or another writer of it is
   outstanding (weight stages, activation slots, A buffers in TMEM, scale
-  slots, accumulators).
+  slots, accumulators);
+- an exit with a copy or an MMA still in flight.
 
 Only tests use this module; it shares nothing with the kernel source beyond
 restating its waits and arrivals.
@@ -99,6 +100,10 @@ class _Sim:
             if not choices:
                 live = [(a["name"], a["wait"]) for a in self.agents if not a["done"]]
                 return f"deadlock: {live[:4]}" if live else None
+            if all(a["done"] for a in self.agents) and (self.inflight or self.commits):
+                # the block would exit (and free its TMEM) with copies or
+                # MMAs still in flight
+                return f"exit with {len(self.inflight)} operations in flight"
             kind, x = self.rng.choice(choices)
             if kind == "o":
                 self.inflight.remove(x)
