@@ -231,7 +231,7 @@ def _roles(c, st):
         for j in range(n):
             if ch.begin(j == 0 or st[j]["g"] == 0):
                 slot, ph = ch.ci % SCALE_SLOTS, (ch.ci // SCALE_SLOTS) & 1
-                if not go and ch.ci >= SCALE_SLOTS:
+                if not go and ch.ci >= SCALE_SLOTS and not c.get("no_early_x_go"):
                     yield ("arrive", "x_go")
                     go = True
                 yield ("wait", f"sempty{slot}", ph ^ 1)

@@ -81,3 +81,14 @@ def test_waiting_for_a_chunk_before_releasing_it_fixes_one_group_tiles(name):
     for the chunk to land before it releases it."""
     cfg = dict(CONFIGS[name], release_after_landing=True)
     assert failures(cfg, ONE_GROUP + RANGES[:3], 40) == {}
+
+
+def test_weights_released_before_a_full_scale_ring_blocks():
+    """Weight-only formats hold the weight stream back until the first
+    activation tiles are queued (x_go).  With one-step segments the scale
+    ring fills first and drains only as the weights flow, so the activation
+    producer releases x_go before it waits on a full scale ring; without
+    that release the block stops."""
+    cfg = dict(CONFIGS["W4A16 T16 two-group"], no_early_x_go=True)
+    assert failures(cfg, [(0, 9, 1), (0, 24, 1)], 10) != {}
+    assert failures(CONFIGS["W4A16 T16 two-group"], [(0, 9, 1), (0, 24, 1)], 10) == {}
