@@ -13,7 +13,7 @@ patterns):
 * ``pack_gptq(q, bits)``              -> (qweight int32, qzeros int32, n_out_of_range)
 * ``unpack_gptq(qweight, K, N, bits)``-> q int8 [K,N]
 * ``group_partials_i8(qa, qweight, K)``-> P int32 [G,M,N]
-* ``gemm_w8a8_gs128(...)``            -> dict of y_bf16 / y_f32 / y64 / bound
+* ``gemm_w8a8_gs128(...)``            -> dict of y_bf16 / y_f32 / y64 / bound / abs_sum
 * ``gemm_w4a16_g128(...)``            -> same dict
 * ``gemm_w8a16(..., group_size)``     -> same dict (int8 weight-only; g32, g128 or per channel)
 * ``dequant_w4a16(qweight, scales, K, N)`` -> w bf16 bits [K,N]
@@ -78,10 +78,10 @@ def _load():
             lib.orc_unpack_gptq.restype = None
             lib.orc_group_partials_i8.argtypes = [P, P, I, I, I, P]
             lib.orc_group_partials_i8.restype = None
-            gemm_args = [P, P, P, P, I, I, I, P, I, P, I, P, P, P, P]
+            gemm_args = [P, P, P, P, I, I, I, P, I, P, I, P, P, P, P, P]
             lib.orc_gemm_w8a8_gs128.argtypes = gemm_args
             lib.orc_gemm_w8a8_gs128.restype = None
-            lib.orc_gemm_w4a16_g128.argtypes = [P, P, P, I, I, I, P, I, P, I, P, P, P, P]
+            lib.orc_gemm_w4a16_g128.argtypes = [P, P, P, I, I, I, P, I, P, I, P, P, P, P, P]
             lib.orc_gemm_w4a16_g128.restype = None
             lib.orc_dequant_w4a16.argtypes = [P, P, I, I, P]
             lib.orc_dequant_w4a16.restype = None
@@ -89,7 +89,7 @@ def _load():
             lib.orc_argmax_bf16_rows.restype = None
             lib.orc_ingest_nk.argtypes = [P, P, I, I, ctypes.c_int, P, P]
             lib.orc_ingest_nk.restype = None
-            lib.orc_gemm_w8a16.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, P, P]
+            lib.orc_gemm_w8a16.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, P, P, P]
             lib.orc_gemm_w8a16.restype = None
             lib.orc_f64_to_bf16.argtypes = [ctypes.c_double]
             lib.orc_f64_to_bf16.restype = ctypes.c_uint16
@@ -178,6 +178,7 @@ def _outputs(nr, nc):
         "y_f32": np.empty((nr, nc), np.float32),
         "y64": np.empty((nr, nc), np.float64),
         "bound": np.empty((nr, nc), np.float64),
+        "abs_sum": np.empty((nr, nc), np.float64),
     }
 
 
@@ -198,7 +199,8 @@ def gemm_w8a8_gs128(qa, sa, qweight, scales_f16_bits, K, rows=None, cols=None):
     _load().orc_gemm_w8a8_gs128(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sc), M, N, K,
                                 _ptr(r), r.size, _ptr(c), c.size,
                                 _ptr(out["y_bf16"]), _ptr(out["y_f32"]),
-                                _ptr(out["y64"]), _ptr(out["bound"]))
+                                _ptr(out["y64"]), _ptr(out["bound"]),
+                                _ptr(out["abs_sum"]))
     return out
 
 
@@ -218,7 +220,8 @@ def gemm_w4a16_g128(x_bits, qweight, scales_bf16_bits, K, rows=None, cols=None):
     _load().orc_gemm_w4a16_g128(_ptr(x), _ptr(qw), _ptr(sc), M, N, K,
                                 _ptr(r), r.size, _ptr(c), c.size,
                                 _ptr(out["y_bf16"]), _ptr(out["y_f32"]),
-                                _ptr(out["y64"]), _ptr(out["bound"]))
+                                _ptr(out["y64"]), _ptr(out["bound"]),
+                                _ptr(out["abs_sum"]))
     return out
 
 
@@ -238,7 +241,8 @@ def gemm_w8a16(x_bits, qweight, scales_bf16_bits, K, group_size, rows=None, cols
     _load().orc_gemm_w8a16(_ptr(x), _ptr(qw), _ptr(sc), M, N, K, int(group_size),
                            _ptr(r), r.size, _ptr(c), c.size,
                            _ptr(out["y_bf16"]), _ptr(out["y_f32"]),
-                           _ptr(out["y64"]), _ptr(out["bound"]))
+                           _ptr(out["y64"]), _ptr(out["bound"]),
+                                _ptr(out["abs_sum"]))
     return out
 
 

@@ -198,12 +198,15 @@ void orc_group_partials_i8(const int8_t *qa, const int32_t *qweight,
  *   y_f32  : acc * sa[m] with acc = fma(P_g, sw[g, n], acc) over g ascending,
  *   y64    : sa[m] * sum_g P_g * sw[g, n] in fp64,
  *   bound  : (G + 2) * 2^-24 * |sa[m]| * sum_g |P_g * sw[g, n]|,
- *            a bound on |y_f32 - y64| for any summation order of the G terms. */
+ *            a bound on |y_f32 - y64| for any summation order of the G terms,
+ *   abs_sum: |sa[m]| * sum_g |P_g * sw[g, n]| in fp64 (the size of the terms,
+ *            against which cancellation in y is measured). */
 void orc_gemm_w8a8_gs128(const int8_t *qa, const float *sa, const int32_t *qweight,
                          const uint16_t *scales_f16, int64_t M, int64_t N, int64_t K,
                          const int64_t *rows, int64_t nrows,
                          const int64_t *cols, int64_t ncols,
-                         uint16_t *y_bf16, float *y_f32, double *y64, double *bound)
+                         uint16_t *y_bf16, float *y_f32, double *y64, double *bound,
+                         double *abs_sum)
 {
     const int64_t G = K / GROUP;
     (void)M;
@@ -228,6 +231,7 @@ void orc_gemm_w8a8_gs128(const int8_t *qa, const float *sa, const int32_t *qweig
             y_bf16[o] = orc_f32_to_bf16(y);
             y64[o] = exact * (double)sa[m];
             bound[o] = (double)(G + 2) * ldexp(1.0, -24) * magnitude * fabs((double)sa[m]);
+            abs_sum[o] = magnitude * fabs((double)sa[m]);
         }
     }
 }
@@ -240,12 +244,13 @@ void orc_gemm_w8a8_gs128(const int8_t *qa, const float *sa, const int32_t *qweig
  * ascending (each product is exact in fp32); y_bf16 = bf16(y_f32);
  * y64 = the same sum in fp64; bound = (K + 2) * 2^-23 * sum_k |x * w|, a
  * bound on |y_f32 - y64| that also covers accumulators that truncate instead
- * of rounding. */
+ * of rounding; abs_sum = sum_k |x * w| in fp64. */
 void orc_gemm_w4a16_g128(const uint16_t *x, const int32_t *qweight,
                          const uint16_t *scales_bf16, int64_t M, int64_t N, int64_t K,
                          const int64_t *rows, int64_t nrows,
                          const int64_t *cols, int64_t ncols,
-                         uint16_t *y_bf16, float *y_f32, double *y64, double *bound)
+                         uint16_t *y_bf16, float *y_f32, double *y64, double *bound,
+                         double *abs_sum)
 {
     (void)M;
     for (int64_t r = 0; r < nrows; ++r) {
@@ -268,6 +273,7 @@ void orc_gemm_w4a16_g128(const uint16_t *x, const int32_t *qweight,
             y_bf16[o] = orc_f32_to_bf16(acc);
             y64[o] = exact;
             bound[o] = (double)(K + 2) * ldexp(1.0, -23) * magnitude;
+            abs_sum[o] = magnitude;
         }
     }
 }
@@ -329,11 +335,12 @@ void orc_ingest_nk(const int32_t *packed_nk, const uint16_t *scales_ng, int64_t 
  * exact product), y = bf16(sum_k x[m, k] * w[k, n]) accumulated in fp32 over
  * k ascending.  q comes from the 8-bit GPTQ words ([K/4, N], byte = q + 128);
  * scales are bf16 [K/gs, N], with gs = 0 meaning one scale per output column
- * (scales [1, N]).  y64 / bound as for W4A16. */
+ * (scales [1, N]).  y64 / bound / abs_sum as for W4A16. */
 void orc_gemm_w8a16(const uint16_t *x, const int32_t *qweight, const uint16_t *scales_bf16,
                     int64_t M, int64_t N, int64_t K, int64_t gs,
                     const int64_t *rows, int64_t nrows, const int64_t *cols, int64_t ncols,
-                    uint16_t *y_bf16, float *y_f32, double *y64, double *bound)
+                    uint16_t *y_bf16, float *y_f32, double *y64, double *bound,
+                    double *abs_sum)
 {
     (void)M;
     for (int64_t r = 0; r < nrows; ++r) {
@@ -357,6 +364,7 @@ void orc_gemm_w8a16(const uint16_t *x, const int32_t *qweight, const uint16_t *s
             y_bf16[o] = orc_f32_to_bf16(acc);
             y64[o] = exact;
             bound[o] = (double)(K + 2) * ldexp(1.0, -23) * magnitude;
+            abs_sum[o] = magnitude;
         }
     }
 }
