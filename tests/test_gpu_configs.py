@@ -82,7 +82,7 @@ def run_w4a16(name, M, K, N, seed=0):
     rows, cols = sample_rows(M, seed), sample_cols(N, seed)
     y = from_dev_bits(y_d)[np.ix_(rows, cols)]
     ref = oracle.gemm_w4a16_g128(xb, qw, sb, K, rows, cols)
-    return compare_linear(y, ref, f"{name} w4a16 M={M}")
+    return compare_linear(y, ref, f"{name} w4a16 M={M}", "w4a16", K)
 
 
 def test_single_w8a8_linear_all_outputs():
@@ -153,7 +153,7 @@ def run_w8a16(name, M, K, N, seed=0, gs=32):
     rows, cols = sample_rows(M, seed), sample_cols(N, seed)
     y = from_dev_bits(y_d)[np.ix_(rows, cols)]
     ref = oracle.gemm_w8a16(xb, qw, sb, K, gs, rows, cols)
-    return compare_linear(y, ref, f"{name} w8a16 M={M}")
+    return compare_linear(y, ref, f"{name} w8a16 M={M}", "w8a16", K)
 
 
 @pytest.mark.parametrize("M", [8, 64])

@@ -190,7 +190,7 @@ def test_w4a16_wide_range_bf16_scales():
     rng = np.random.default_rng(22)
     sb = synth.bf16_bits(np.exp2(rng.uniform(-30.0, 30.0, size=(K // 128, N))))
     y = _gemm_w4a16_gpu(xb, qw, sb)
-    compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), "w4a16 wide scales")
+    compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), "w4a16 wide scales", "w4a16", K)
 
 
 def test_w8a8_identity_probe():
@@ -228,7 +228,7 @@ def test_shared_workspace_across_shapes():
         compare_linear(y, oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K), f"shared ws w8a8 {i}")
         xb, _, qw4, sb = _w4a16_inputs(60 + i, f"gpu/w4/shared/{i}", M, K, N)
         y4 = _gemm_w4a16_gpu(xb, qw4, sb, ws)
-        compare_linear(y4, oracle.gemm_w4a16_g128(xb, qw4, sb, K), f"shared ws w4a16 {i}")
+        compare_linear(y4, oracle.gemm_w4a16_g128(xb, qw4, sb, K), f"shared ws w4a16 {i}", "w4a16", K)
     assert not ws.buf[:4096].view(torch.int32).cpu().numpy().any()
 
 
@@ -253,11 +253,14 @@ def _gemm_w4a16_gpu(xb, qw, sb, workspace=None):
     (96, 1280, 384), (130, 512, 264),
     # one (two-group) step per tile: every step opens its own scale chunk
     (8, 128, 2048), (8, 256, 2048), (64, 256, 4096),
+    # one-group tiles on every SM, many chunks per block: 16-, 32- and
+    # 64-token tiles, where a converter group could run chunks ahead
+    (8, 128, 40960), (32, 128, 40960), (64, 128, 40960), (64, 256, 40960),
 ])
 def test_w4a16_matches_oracle(M, K, N):
     xb, _, qw, sb = _w4a16_inputs(9, f"gpu/w4/{M}/{K}/{N}", M, K, N)
     y = _gemm_w4a16_gpu(xb, qw, sb)
-    compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), f"w4a16 {M}x{K}x{N}")
+    compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), f"w4a16 {M}x{K}x{N}", "w4a16", K)
 
 
 @pytest.mark.parametrize("fmt,M", [("w8a8", 8), ("w8a8", 64), ("w8a8", 96), ("w4a16", 8), ("w4a16", 64)])
@@ -287,7 +290,8 @@ def test_fused_projections_match_each_oracle(fmt, M):
     for i, ((qw, sc), N) in enumerate(zip(parts, Ns)):
         ref = (oracle.gemm_w8a8_gs128(qa, sa, qw, sc, K) if fmt == "w8a8"
                else oracle.gemm_w4a16_g128(xb, qw, sc, K))
-        compare_linear(np.ascontiguousarray(y[:, off:off + N]), ref, f"fused {fmt} M={M} part {i}")
+        compare_linear(np.ascontiguousarray(y[:, off:off + N]), ref, f"fused {fmt} M={M} part {i}",
+                       fmt, K)
         off += N
 
 
@@ -307,7 +311,7 @@ def test_w4a16_full_nibble_range():
     qw, _, _ = oracle.pack_gptq(qwt, 4)
     sb = synth.bf16_bits(synth.log_uniform(11, "gpu/w4/nib/s", (K // 128, N), 1e-3, 3e-2))
     y = _gemm_w4a16_gpu(xb, qw, sb)
-    compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), "w4a16 nibble range")
+    compare_linear(y, oracle.gemm_w4a16_g128(xb, qw, sb, K), "w4a16 nibble range", "w4a16", K)
 
 
 # ------------------------------------------------------------ host checks
@@ -435,7 +439,8 @@ def test_w4a16_from_ingested_weights_matches_oracle():
     qw_d, sb_d = qlin.ingest_nk(to_dev(packed), to_dev_bits(sb_ng, torch.bfloat16), K, 4)
     y = qlin.gemm_w4a16_g128(to_dev_bits(xb, torch.bfloat16), qw_d, sb_d)
     torch.cuda.synchronize()
-    compare_linear(from_dev_bits(y), oracle.gemm_w4a16_g128(xb, qw, sb, K), "ingested w4a16")
+    compare_linear(from_dev_bits(y), oracle.gemm_w4a16_g128(xb, qw, sb, K), "ingested w4a16",
+                   "w4a16", K)
 
 
 # ------------------------------------------------------ W8A16 (int8 weight-only)
@@ -449,12 +454,14 @@ def _w8a16_inputs(seed, name, M, K, N, gs):
 
 @pytest.mark.parametrize("gs", [32, 128, 0])
 @pytest.mark.parametrize("M,K,N", [(1, 128, 128), (8, 5120, 1024), (17, 640, 264), (64, 1280, 384),
-                                   (96, 384, 136), (130, 256, 200), (8, 128, 2048)])
+                                   (96, 384, 136), (130, 256, 200), (8, 128, 2048),
+                                   (8, 128, 40960), (64, 256, 40960)])
 def test_w8a16_matches_oracle(M, K, N, gs):
     xb, qw, sb = _w8a16_inputs(16, f"gpu/w8a16/{M}/{K}/{N}/{gs}", M, K, N, gs)
     y = qlin.gemm_w8a16(to_dev_bits(xb, torch.bfloat16), to_dev(qw), to_dev_bits(sb, torch.bfloat16), gs)
     torch.cuda.synchronize()
-    compare_linear(from_dev_bits(y), oracle.gemm_w8a16(xb, qw, sb, K, gs), f"w8a16 g{gs} {M}x{K}x{N}")
+    compare_linear(from_dev_bits(y), oracle.gemm_w8a16(xb, qw, sb, K, gs), f"w8a16 g{gs} {M}x{K}x{N}",
+                   "w8a16", K)
 
 
 @pytest.mark.parametrize("gs", [32, 0])
@@ -482,7 +489,10 @@ def test_w8a16_rejects_other_group_sizes():
 
 @pytest.mark.parametrize("fmt,M,K,N", [("w4a16", 8, 5120, 17408), ("w4a16", 8, 4096, 5120),
                                        ("w4a16", 64, 17408, 5120), ("w8a8", 8, 5120, 17408),
-                                       ("w8a8", 96, 5120, 6144), ("w8a16", 8, 5120, 6144)])
+                                       ("w8a8", 96, 5120, 6144), ("w8a16", 8, 5120, 6144),
+                                       # tiles of one K group: every scale chunk is one step
+                                       ("w4a16", 8, 128, 622592), ("w4a16", 64, 128, 622592),
+                                       ("w8a16", 8, 128, 622592)])
 def test_repeated_launches_are_identical(fmt, M, K, N):
     """Hundreds of launches of one full-size linear, back to back on one
     stream with one workspace: no bounded wait may run out, and every launch

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import bf16_ulp, compare_linear, from_dev_bits, to_dev, to_dev_bits
+from helpers import compare_linear, from_dev_bits, to_dev, to_dev_bits
 from w4a16_linear_layers_gb300 import build as qbuild
 from w4a16_linear_layers_gb300 import qlin, synth
 
@@ -58,17 +58,20 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row(lib):
         assert st == qlin.QLIN_OK, qlin.status_string(st)
         y_ws = qlin.gemm_w8a8_gs128(qa_d, sa_d, qw_d, sc_d)
         torch.cuda.synchronize()
-        a = synth.bf16_values(from_dev_bits(y_na)).astype(np.float64)
-        b = synth.bf16_values(from_dev_bits(y_ws)).astype(np.float64)
-        # same tolerance as every output check: within 1 bf16 ulp
-        assert np.all(np.abs(a - b) <= bf16_ulp(b)), f"call {seed}: no-alloc differs from workspace entry"
+        # the same kernel with the same plan and the same split of K: the
+        # outputs must be identical bit for bit (a stale partial or counter
+        # left in the shared array would show here)
+        assert np.array_equal(from_dev_bits(y_na), from_dev_bits(y_ws)), \
+            f"call {seed}: no-alloc differs from workspace entry"
         compare_linear(from_dev_bits(y_na), oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K),
                        f"no-alloc call {seed}")
     assert qlin.device_status() == qlin.QLIN_OK
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lib):
-    M, K, N = 8192, 1024, 1024          # 128-token tiles and a 16 MiB activation image
+    # 96-token tiles: the 16 MiB fp16 activation image plus the per-block
+    # split partials (about 15 MB on 152 SMs) exceed the 24 MiB array
+    M, K, N = 8192, 1024, 1024
     assert qlin.workspace_bytes(M, N, K) > 24 * 1024 * 1024
     qa_d = torch.zeros((M, K), dtype=torch.int8, device="cuda")
     sa_d = torch.zeros(M, dtype=torch.float32, device="cuda")
