@@ -254,7 +254,7 @@ qlin_status_t qlin_gemm_w8a16(const uint16_t *x, const int32_t *qweight, const u
  *
  *   arguments as for the matching GEMM, except:
  *   argmax   int32 [M]             device; 4-byte aligned
- *   M        at most 128 (one token tile); larger M returns QLIN_ERR_SHAPE
+ *   M        at most 96 (one token tile); larger M returns QLIN_ERR_SHAPE
  *   workspace / workspace_bytes    at least qlin_workspace_bytes(M, N, K)
  *
  * Each output value is the bit-identical bf16 value the matching GEMM call

@@ -316,7 +316,7 @@ def _roles(c, st):
                 yield ("arrive", f"afull{ab}")
             if WO and ch.ends(st[j]["last"]):
                 slot = ch.ci % SCALE_SLOTS
-                if c.get("release_after_landing") and not ready:
+                if not c.get("release_without_landing") and not ready:
                     yield ("wait", f"sfull{slot}", (ch.ci // SCALE_SLOTS) & 1)
                 yield ("arrive", f"sempty{slot}")
             ch.advance()

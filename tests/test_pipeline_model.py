@@ -49,7 +49,7 @@ def failures(cfg, ranges, seeds):
 @pytest.mark.parametrize("name", sorted(CONFIGS))
 def test_configurations_have_no_deadlock_or_hazard(name):
     cfg = CONFIGS[name]
-    ranges = RANGES + (ONE_GROUP if cfg["mode"] != "wo" or cfg["NB"] == 2 else [])
+    ranges = RANGES + ONE_GROUP
     assert failures(cfg, ranges, 25) == {}
 
 
@@ -63,24 +63,24 @@ def test_an_odd_a_buffer_count_breaks_the_protocol():
     assert failures(cfg, [(6, 24, 20), (0, 40, 20)], 60) != {}
 
 
-@pytest.mark.xfail(strict=True, reason="open: weight-only tiles of one K group with more than "
-                                       "two A buffers (K = 128, or K = 256 with one group a step)")
+@pytest.mark.parametrize("name", ["W4A16 T16", "W4A16 T64", "W8A16 T16"])
+def test_releasing_a_chunk_without_waiting_breaks_one_group_tiles(name):
+    """Tiles of one 128-wide group make every scale chunk one step long.  If
+    a converter warp released a chunk it had no step in without waiting for
+    it to land, a group running four chunks ahead would add its releases to
+    an earlier chunk's phase: the scale slot would be reloaded under a warp
+    that still reads it (or the pipeline would stop).  The kernel's converter
+    warps therefore wait for every chunk before they release it; this is the
+    protocol without that wait."""
+    cfg = dict(CONFIGS[name], release_without_landing=True)
+    assert failures(cfg, ONE_GROUP, 60) != {}
+
+
 @pytest.mark.parametrize("name", ["W4A16 T16", "W4A16 T64", "W8A16 T16"])
 def test_one_group_tiles_weight_only(name):
-    """Tiles of one 128-wide group make every scale chunk one step long.  A
-    converter warp releases a chunk it had no step in without waiting for it,
-    so a group running four chunks ahead adds its releases to an earlier
-    chunk's phase: the scale slot is reloaded under a warp that still reads it
-    (or the pipeline stops).  Shapes with K = 128 hit it."""
-    assert failures(CONFIGS[name], ONE_GROUP, 60) == {}
-
-
-@pytest.mark.parametrize("name", ["W4A16 T16", "W4A16 T64", "W8A16 T16"])
-def test_waiting_for_a_chunk_before_releasing_it_fixes_one_group_tiles(name):
-    """The fix for the case above: a warp that had no step in a chunk waits
-    for the chunk to land before it releases it."""
-    cfg = dict(CONFIGS[name], release_after_landing=True)
-    assert failures(cfg, ONE_GROUP + RANGES[:3], 40) == {}
+    """The same one-group tiles with the kernel's protocol (wait for the
+    chunk to land, then release it): no deadlock and no hazard."""
+    assert failures(CONFIGS[name], ONE_GROUP + RANGES[:3], 60) == {}
 
 
 def test_weights_released_before_a_full_scale_ring_blocks():

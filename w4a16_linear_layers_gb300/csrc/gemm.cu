@@ -775,9 +775,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if constexpr (C::kWO) {
-        // both groups release each scale chunk (a group that had no step in it
-        // read nothing from it)
+        // Both groups release each scale chunk.  A group that had no step in
+        // the chunk read nothing from it, but it still waits for the chunk to
+        // land first: with one-step chunks (tiles of one K group) a group
+        // could otherwise run several chunks ahead, complete an earlier
+        // chunk's release phase in the other group's place, and let the
+        // producer reload a slot that the other group still reads.
         if (ch.ends(seg_last)) {
+          if (!chunk_ready &&
+              !warp_all(mbar_wait(smem_u32(&ctrl->s_full[ch.ci % SR]),
+                                  static_cast<uint32_t>(ch.ci / SR) & 1u, ctx, 20)))
+            break;
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ctrl->s_empty[ch.ci % SR]));
         }
@@ -1188,8 +1196,7 @@ cudaError_t launch_mode(const GemmArgs& a, const GemmPlan& pl, int* err, cudaStr
       if (kMode == kModeW4 && a.K % 256 == 0 && pl.TT * pl.F * (pl.G / 2) >= 16 * pl.ctas)
         return launch_t<kMode, 64, kMode == kModeW4 ? 2 : 1>(a, pl, err, stream);
       return launch_t<kMode, 64, 1>(a, pl, err, stream);
-    case 96: return launch_t<kMode, 96, 1>(a, pl, err, stream);
-    default: return launch_t<kMode, 128, 1>(a, pl, err, stream);
+    default: return launch_t<kMode, 96, 1>(a, pl, err, stream);
   }
 }
 
@@ -1203,10 +1210,11 @@ cudaError_t launch_argmax_finalize(const unsigned long long* keys, int64_t M, in
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
   GemmPlan p{};
-  // 96-token tiles also for large batches: at M = 2048 and 8192 they ran the
-  // W8A8 MLP projections 3-12% faster than 128-token tiles (more D buffers
-  // per group for the per-group rescale), ragged last tile included
-  p.T = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 96 ? 96 : M >= 1024 ? 96 : 128;
+  // Batches above 64 rows take 96-token tiles.  128-token tiles are not
+  // planned: at M = 2048 and 8192 they ran the W8A8 MLP projections 3-12%
+  // slower (two D buffers per group instead of four), and graph replays of
+  // the 128-token-tile path ended in an unexplained launch failure.
+  p.T = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 96;
   p.F = (N + kTileF - 1) / kTileF;
   p.TT = (M + p.T - 1) / p.T;
   p.G = K / kGroup;

@@ -60,10 +60,10 @@ struct GemmArgs {
   int group_size = 128;
 };
 
-// Offset of the argmax keys (one per row, M <= 128) inside the fixed counter
+// Offset of the argmax keys (one per row, M <= 96) inside the fixed counter
 // region at the start of the workspace.
 constexpr size_t kArgmaxKeysOffset = 4096;
-constexpr int64_t kArgmaxMaxRows = 128;
+constexpr int64_t kArgmaxMaxRows = 96;
 
 // idx[m] = the column index encoded in keys[m] (-1 if no key).  Programmatic
 // dependent launch: waits for the GEMM that produced the keys.
@@ -72,7 +72,7 @@ cudaError_t launch_argmax_finalize(const unsigned long long* keys, int64_t M, in
 
 // Tiling plan for one GEMM call.
 struct GemmPlan {
-  int T;           // token tile (MMA N): 16, 32, 64, 96 or 128
+  int T;           // token tile (MMA N): 16, 32, 64 or 96
   int64_t F;       // feature tiles of 128
   int64_t TT;      // token tiles
   int64_t G;       // groups of 128 along K

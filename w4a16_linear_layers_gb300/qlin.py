@@ -331,7 +331,7 @@ def gemm_w8a16(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, gro
 def gemm_w8a8_gs128_argmax(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
                            scales: torch.Tensor, out: torch.Tensor | None = None,
                            workspace=None, stream=None) -> torch.Tensor:
-    """Greedy token per row of the W8A8 GS128 linear (M <= 128): int32 [M],
+    """Greedy token per row of the W8A8 GS128 linear (M <= 96): int32 [M],
     the index of the largest bf16 output, lowest index on ties."""
     _need(q_a, "q_a", torch.int8, 2)
     _need(s_a, "s_a", torch.float32, 1)
@@ -354,7 +354,7 @@ def gemm_w8a8_gs128_argmax(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.
 def gemm_w4a16_g128_argmax(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
                            out: torch.Tensor | None = None, workspace=None,
                            stream=None) -> torch.Tensor:
-    """Greedy token per row of the W4A16 g128 linear (M <= 128)."""
+    """Greedy token per row of the W4A16 g128 linear (M <= 96)."""
     _need(x, "x", torch.bfloat16, 2)
     _need(qweight, "qweight", torch.int32, 2)
     _need(scales, "scales", torch.bfloat16, 2)
