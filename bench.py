@@ -1,15 +1,30 @@
 """Benchmark of the group-wise quantized linear layer on GB300.
 
-Default workload (one JSON line on stdout): one DFlash2 drafter layer's seven
-W8A8 GS128 projections (q 5120->4096, k/v 5120->1024, o 4096->5120, gate/up
-5120->17408, down 17408->5120) at M = 8*C tokens for C in {1, 8, 12}
-(M = 8, 64, 96).  One step = for each M: dynamic INT8 quantization of the
-four distinct layer inputs, then the seven GEMMs (12 + 21 kernel launches),
-replayed as one CUDA graph.  Metric: weight GB/s (qweight + scale bytes
-streamed per step / step time); TOPS is reported beside it.
+Default run (one JSON line on stdout): every workload configuration of the
+layer, the drafter layer as the headline and the others as keyed sub-records
+under "configs":
+
+  layer    one DFlash2 drafter layer's seven W8A8 GS128 projections (q
+           5120->4096, k/v 5120->1024, o 4096->5120, gate/up 5120->17408,
+           down 17408->5120) at M = 8*C tokens for C in {1, 8, 12}
+           (M = 8, 64, 96)  [headline]
+  single   one W8A8 GS128 linear 5120->1024 at M = 8
+  drafter  the full drafter, 35 W8A8 GS128 linears + fc 25600->5120, M = 96
+  w4a16    the same 36 shapes in W4A16 g128, M in {8, 64}
+  prefill  W8A8 gate/up 5120->17408 and down 17408->5120 at M in {128, 512,
+           2048, 8192} (tensor-bound at M >= 2048)
+  vocab    the W8A8 GS128 vocabulary head 5120->248320 at M in {8, 96}
+
+One step of a workload = dynamic INT8 quantization of its distinct inputs
+(W8A8), then its GEMMs, replayed as one CUDA graph.  Metric: weight GB/s
+(qweight + scale bytes streamed per step / step time), TOPS beside it; the
+prefill record reports TOPS.  Each record carries its own roofline (the
+GEMM launches alone), end-to-end rate through the binding with host copies,
+and the oracle timed on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload layer|single|drafter|w4a16|prefill|vocab]
+                    [--workload all|layer|single|drafter|w4a16|w8a16|prefill|
+                                vocab|vocab_argmax|producers]
 
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload on its own GPU (the layer has no exchange step on one GPU);
@@ -18,7 +33,9 @@ value = total over ranks / max time over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -35,12 +52,14 @@ if ROOT not in sys.path:
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+LARGE_M = 2048          # prefill batches at and above this are tensor-bound
 
 
 # ------------------------------------------------------------------ workloads
 
 def workload_specs(name: str):
-    """List of (linear name, K, N, activation kind, M, kind 'w8a8'|'w4a16')."""
+    """List of (linear name, K, N, activation kind, M, kind 'w8a8'|'w4a16'|...)."""
     from w4a16_linear_layers_gb300 import synth
 
     specs = []
@@ -90,6 +109,10 @@ WORKLOAD_DESC = {
                  "SiLU(gate)*up over [M,2x17408], M in {8,96,2048,8192}",
 }
 
+# the default run: the headline, then the sub-records (workload configurations)
+HEADLINE = "layer"
+SUB_RECORDS = ("single", "drafter", "w4a16", "prefill", "vocab")
+METRIC = "W8A8-GS128 linear weight GB/s (TOPS beside it); % of HBM / tensor roofline"
 
 W8A16_GROUP = 32   # the bench's W8A16 scale group (the DFlash2 recipe's group-32 int8)
 
@@ -110,6 +133,25 @@ def gemm_algo_bytes(M, K, N, kind):
     kind = kind.replace("_argmax", "")
     act = M * K * (1 if kind == "w8a8" else 2) + (4 * M if kind == "w8a8" else 0)   # w4a16/w8a16: bf16 x
     return weight_bytes(K, N, kind) + act + out
+
+
+def bound_of(name):
+    return "tensor" if name == "prefill" else "hbm"
+
+
+def workload_config(name, fused, world):
+    """The static description of a workload (the same in both arms)."""
+    specs = workload_specs(name)
+    return {
+        "workload": WORKLOAD_DESC[name],
+        "linears_per_step": len(specs),
+        "fused_projections": ("projections that read the same input (q/k/v, gate/up) run as one "
+                              "GEMM over their weights concatenated along N: same bytes and outputs"
+                              if fused else "off: one GEMM per linear"),
+        "weight_bytes_per_step": sum(weight_bytes(K, N, wk) for _, K, N, _, _, wk in specs),
+        "ops_per_step": sum(2 * M * K * N for _, K, N, _, M, _ in specs),
+        "parallelism": f"replicas x{world}",
+    }
 
 
 # -------------------------------------------------------------------- clocks
@@ -174,40 +216,44 @@ class ClockSampler:
 
 
 def measured_peaks():
+    """Roofline denominators: the measured copy bandwidth and bf16
+    tensor rates of this GPU model (MEASURED_PEAKS.json), else fallbacks."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
     except (OSError, KeyError, ValueError):
-        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+        return {"hbm": FALLBACK_HBM_GBS, "bf16": FALLBACK_BF16_TFLOPS,
+                "bf16_sustained": FALLBACK_BF16_TFLOPS_SUSTAINED, "source": "fallback"}
 
 
-def profiled_traffic(workload, fused):
-    """DRAM bytes per GEMM launch from the committed ncu summary of this
-    workload and call list (fused or one GEMM per linear), or None when the
-    GEMM sources changed since that capture (the summary records the sha256
-    prefix of the sources it measured)."""
-    if workload != "layer":
-        return None
-    key = "traffic_bytes_per_launch_fused:" if fused else "traffic_bytes_per_launch:"
-    import hashlib
-    csrc = os.path.join(ROOT, "w4a16_linear_layers_gb300", "csrc")
+def source_hash(names):
     h = hashlib.sha256()
-    for name in ("gemm.cu", "qlin_device.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
+    for name in names:
+        with open(os.path.join(ROOT, "w4a16_linear_layers_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ("gemm.cu", "qlin_device.cuh")
+
+
+def profiled_traffic(key, sources=GEMM_SOURCES):
+    """DRAM bytes per launch of a workload's dominant kernel, from the ncu
+    counters recorded in profiles/traffic.json, or None when that kernel's
+    sources changed since the capture (each entry records the sha256 prefix
+    of the sources it measured)."""
     try:
-        with open(os.path.join(ROOT, "profiles", "gemm_w8a8_drafter_layer_dram.md")) as f:
-            text = f.read()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f).get(key)
+    except (OSError, ValueError):
         return None
-    if h.hexdigest()[:16] not in text:
+    if not entry or entry.get("sources_sha16") != source_hash(sources):
         return None
-    for line in text.splitlines():
-        if line.startswith(key):
-            return int(line.split(":")[1])
-    return None
+    return int(entry["dram_bytes_per_launch"])
 
 
 # ---------------------------------------------------------------- our arm
@@ -218,9 +264,13 @@ class LayerRunner:
     With fuse, projections that read the same input (q/k/v, gate/up) run as
     one GEMM over their weights concatenated along N: the same bytes and
     outputs (output columns are independent), fewer launches.  The unfused
-    call list is kept beside it so both can be timed."""
+    call list is kept beside it so both can be timed.
 
-    def __init__(self, specs, device, seed=0):
+    copies > 1 holds that many distinct copies of the weights, used in turn
+    by consecutive steps, so that a workload whose weights fit in L2 still
+    streams them from HBM every step."""
+
+    def __init__(self, specs, device, seed=0, copies=1):
         import torch
 
         from w4a16_linear_layers_gb300 import qlin, synth
@@ -228,30 +278,15 @@ class LayerRunner:
         self.torch, self.qlin = torch, qlin
         self.specs = specs
         self.device = device
+        self.copies = copies
         self.ws = qlin.Workspace(device)
-        self.weights = {}
+        weights = {}
         self.inputs = {}
         self.acts = {}
         for name, K, N, kind, M, wk in specs:
             key = (name, wk)
-            if key not in self.weights:
-                if wk.startswith("w8a8"):
-                    q, s = synth.w8a8_weights(seed, name, K, N)
-                    qd = torch.from_numpy(q).to(device)
-                    qw, _ = qlin.pack_gptq(qd, 8, with_qzeros=False)
-                    sd = torch.from_numpy(s.view(np.int16)).view(torch.float16).to(device)
-                elif wk == "w8a16":
-                    q, s = synth.w8a16_weights(seed, name + "/w8a16", K, N, W8A16_GROUP)
-                    qd = torch.from_numpy(q).to(device)
-                    qw, _ = qlin.pack_gptq(qd, 8, with_qzeros=False)
-                    sd = torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).to(device)
-                else:
-                    q, s = synth.w4a16_weights(seed, name + "/w4", K, N)
-                    qd = torch.from_numpy(q).to(device)
-                    qw, _ = qlin.pack_gptq(qd, 4, with_qzeros=False)
-                    sd = torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).to(device)
-                del qd
-                self.weights[key] = (qw, sd)
+            if key not in weights:
+                weights[key] = self._weights(name, K, N, wk, seed)
             ikey = self._ikey((name, K, N, kind, M, wk))
             if ikey not in self.inputs:
                 xb = synth.activations(seed, f"{ikey[0]}/M{M}", M, K, kind)
@@ -259,25 +294,57 @@ class LayerRunner:
                 if wk.startswith("w8a8"):
                     self.acts[ikey] = (torch.empty((M, K), dtype=torch.int8, device=device),
                                        torch.empty((M,), dtype=torch.float32, device=device))
-        # unfused: one call per linear; fused: one call per (input, format)
+        # calls[fused][copy]: unfused = one call per linear; fused = one call
+        # per (input, format)
         self.calls = {False: [], True: []}
         groups = {}
         for spec in specs:
-            name, K, N, kind, M, wk = spec
-            self.calls[False].append(self._call(wk, self._ikey(spec), [name], M, K))
-            groups.setdefault((self._ikey(spec), wk), []).append(name)
-        for (ikey, wk), names in groups.items():
-            self.calls[True].append(self._call(wk, ikey, names, ikey[1], ikey[2]))
+            groups.setdefault((self._ikey(spec), spec[5]), []).append(spec[0])
+        for c in range(copies):
+            self.calls[False].append([self._call(weights, wk, self._ikey(spec), [spec[0]], spec[4],
+                                                 spec[1], c)
+                                      for spec in specs for wk in [spec[5]]])
+            self.calls[True].append([self._call(weights, wk, ikey, names, ikey[1], ikey[2], c)
+                                     for (ikey, wk), names in groups.items()])
+        del weights
         torch.cuda.synchronize()
         self.weight_bytes = sum(weight_bytes(K, N, wk) for _, K, N, _, _, wk in specs)
         self.ops = sum(2 * M * K * N for _, K, N, _, M, _ in specs)
         self.n_actq = len(self.acts)
 
-    def _call(self, wk, ikey, names, M, K):
+    def _weights(self, name, K, N, wk, seed):
+        """Packed weights and scales of one linear, drawn as synth's
+        w8a8_weights / w4a16_weights / w8a16_weights draw them: the integer
+        weights on the device (the same stream, bit for bit), the scales on
+        the host."""
+        torch, qlin = self.torch, self.qlin
+        from w4a16_linear_layers_gb300 import synth
+
+        if wk.startswith("w8a8"):
+            q = synth.randint_device(seed, name + "/qw", (K, N), -127, 127, self.device)
+            s = synth.f16_bits(synth.log_uniform(seed, name + "/sw", (K // 128, N), 1e-3, 1e-2))
+            bits, sdt = 8, torch.float16
+        elif wk == "w8a16":
+            q = synth.randint_device(seed, name + "/w8a16/qw", (K, N), -127, 127, self.device)
+            s = synth.bf16_bits(synth.log_uniform(seed, name + "/w8a16/sw", (K // W8A16_GROUP, N),
+                                                  1e-3, 1e-2))
+            bits, sdt = 8, torch.bfloat16
+        else:
+            q = synth.randint_device(seed, name + "/w4/qw", (K, N), -7, 7, self.device)
+            s = synth.bf16_bits(synth.log_uniform(seed, name + "/w4/sw", (K // 128, N), 1e-3, 3e-2))
+            bits, sdt = 4, torch.bfloat16
+        qw, _ = qlin.pack_gptq(q, bits, with_qzeros=False)
+        del q
+        sd = torch.from_numpy(s.view(np.int16)).view(sdt).to(self.device)
+        return qw, sd
+
+    def _call(self, weights, wk, ikey, names, M, K, copy):
         torch = self.torch
-        parts = [self.weights[(n, wk)] for n in names]
+        parts = [weights[(n, wk)] for n in names]
         if len(parts) == 1:
             qw, sc = parts[0]
+            if copy > 0:
+                qw, sc = qw.clone(), sc.clone()
         else:
             qw = torch.cat([p[0] for p in parts], dim=1).contiguous()
             sc = torch.cat([p[1] for p in parts], dim=1).contiguous()
@@ -292,20 +359,26 @@ class LayerRunner:
         return {"wk": wk, "ikey": ikey, "qw": qw, "sc": sc, "ys": ys, "M": M, "N": N, "K": K,
                 "names": names}
 
-    def outputs(self, fused, buf=0):
-        return [c["ys"][buf] for c in self.calls[fused]]
+    def outputs(self, fused, buf=0, copy=0):
+        return [c["ys"][buf] for c in self.calls[fused][copy]]
 
     def n_gemm(self, fused):
-        return len(self.calls[fused])
+        return len(self.calls[fused][0])
 
-    def gemm_bytes(self, fused):
-        return sum(gemm_algo_bytes(c["M"], c["K"], c["N"], c["wk"]) for c in self.calls[fused])
+    def gemm_bytes(self, fused, sel=None):
+        return sum(gemm_algo_bytes(c["M"], c["K"], c["N"], c["wk"])
+                   for c in self.calls[fused][0] if sel is None or sel(c))
+
+    def gemm_ops(self, fused, sel=None):
+        return sum(2 * c["M"] * c["K"] * c["N"] for c in self.calls[fused][0]
+                   if sel is None or sel(c))
 
     def n_launches(self, fused):
         # one kernel per act-quant and per GEMM, plus the int8 -> fp16 operand
-        # pass of W8A8 GEMMs with token tiles of 96 and more (M > 64)
+        # pass of W8A8 GEMMs with token tiles of 96 (M > 64), plus the argmax
+        # decode
         return self.n_actq + sum(1 + (c["wk"].startswith("w8a8") and c["M"] > 64)
-                                 + c["wk"].endswith("_argmax") for c in self.calls[fused])
+                                 + c["wk"].endswith("_argmax") for c in self.calls[fused][0])
 
     def _ikey(self, spec):
         from w4a16_linear_layers_gb300 import synth
@@ -317,26 +390,32 @@ class LayerRunner:
         for ikey, (q, s) in self.acts.items():
             self.qlin.act_quant_i8(self.inputs[ikey], q, s)
 
-    def gemms(self, fused=False, buf=0):
+    def gemms(self, fused=False, buf=0, copy=0, sel=None):
         ws = self.ws.buf
-        for c in self.calls[fused]:
-            c["y"] = c["ys"][buf]
+        for c in self.calls[fused][copy]:
+            if sel is not None and not sel(c):
+                continue
+            y = c["ys"][buf]
             if c["wk"] == "w8a8_argmax":
                 q, s = self.acts[c["ikey"]]
-                self.qlin.gemm_w8a8_gs128_argmax(q, s, c["qw"], c["sc"], c["y"], workspace=ws)
+                self.qlin.gemm_w8a8_gs128_argmax(q, s, c["qw"], c["sc"], y, workspace=ws)
             elif c["wk"] == "w8a8":
                 q, s = self.acts[c["ikey"]]
-                self.qlin.gemm_w8a8_gs128(q, s, c["qw"], c["sc"], c["y"], workspace=ws)
+                self.qlin.gemm_w8a8_gs128(q, s, c["qw"], c["sc"], y, workspace=ws)
             elif c["wk"] == "w8a16":
-                self.qlin.gemm_w8a16(self.inputs[c["ikey"]], c["qw"], c["sc"], W8A16_GROUP, c["y"],
+                self.qlin.gemm_w8a16(self.inputs[c["ikey"]], c["qw"], c["sc"], W8A16_GROUP, y,
                                      workspace=ws)
             else:
-                self.qlin.gemm_w4a16_g128(self.inputs[c["ikey"]], c["qw"], c["sc"], c["y"],
+                self.qlin.gemm_w4a16_g128(self.inputs[c["ikey"]], c["qw"], c["sc"], y,
                                           workspace=ws)
 
-    def step(self, fused=False, buf=0):
+    def step(self, fused=False, buf=0, copy=0):
         self.quantize()
-        self.gemms(fused, buf)
+        self.gemms(fused, buf, copy)
+
+    def all_copies(self, fn):
+        for c in range(self.copies):
+            fn(c)
 
     def capture(self, fn):
         torch = self.torch
@@ -384,62 +463,58 @@ def time_graph(torch, graph, reps):
     return start.elapsed_time(end) / 1e3  # seconds
 
 
-# Workloads whose CUDA-graph replay is disabled: the prefill graph (W8A8 GEMMs
-# with 128-token tiles, M up to 8192) faulted the GPU after tens of
-# back-to-back replays while every single replay, and every shape run alone,
-# passed.  Until the cause is found it is not replayed; its shapes stay
-# covered by the parity tests (eager calls).
-DISABLED_WORKLOADS = {
-    "prefill": "graph replay of the prefill step faulted the GPU (unspecified launch "
-               "failure after tens of back-to-back replays); disabled until the cause is found",
-}
-
-
-def run_ours(args, rank, world, local_rank):
-    if args.workload in DISABLED_WORKLOADS:
-        raise SystemExit(f"workload {args.workload!r} is disabled: {DISABLED_WORKLOADS[args.workload]}")
+def measure(name, args, device, world, steps, fused=True, with_alt=False, clocks=None):
+    """Time one workload: its step graph (act-quants + GEMMs), its GEMM
+    launches alone (the roofline kernel), the end-to-end leg through the
+    binding with host copies, and, for the headline, the other call list.
+    `clocks`, if given, samples the SM clocks from the soak to the end of the
+    timed replays.  Returns (record without the oracle baseline, runner)."""
     import torch
-    from w4a16_linear_layers_gb300 import build as qbuild
+
     from w4a16_linear_layers_gb300 import qlin
 
-    qbuild.build()
-    device = torch.device(f"cuda:{local_rank}")
-    torch.cuda.set_device(device)
-    specs = workload_specs(args.workload)
-    runner = LayerRunner(specs, device)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-    fused = not args.no_fuse
-    step_graph = runner.capture(lambda: runner.step(fused))
-    gemm_graph = runner.capture(lambda: runner.gemms(fused))
-    # the other call list (unfused when the headline is fused), timed beside it
-    alt_graph = runner.capture(lambda: runner.step(not fused)) if runner.n_gemm(True) != runner.n_gemm(False) else None
-    # Bring the clocks up from idle before the warm-up proper (untimed).
+    specs = workload_specs(name)
+    wbytes = sum(weight_bytes(K, N, wk) for _, K, N, _, _, wk in specs)
+    # weights that fit in L2 rotate through distinct copies, three L2s' worth
+    copies = 1 if wbytes >= 2 * L2_BYTES else int(math.ceil(3 * L2_BYTES / wbytes))
+    runner = LayerRunner(specs, device, copies=copies)
+    # the roofline kernel: every GEMM of the step, or for the tensor-bound
+    # prefill the batches of LARGE_M rows and more
+    sel = (lambda c: c["M"] >= LARGE_M) if bound_of(name) == "tensor" else None
+    step_graph = runner.capture(lambda: runner.all_copies(lambda c: runner.step(fused, 0, c)))
+    gemm_graph = runner.capture(lambda: runner.all_copies(lambda c: runner.gemms(fused, 0, c, sel)))
+    alt_graph = None
+    if with_alt and runner.n_gemm(True) != runner.n_gemm(False):
+        alt_graph = runner.capture(lambda: runner.all_copies(lambda c: runner.step(not fused, 0, c)))
+    if clocks is not None:
+        clocks.start()
     t_soak = time.perf_counter()
     while time.perf_counter() - t_soak < args.soak:
-        for _ in range(20):
-            step_graph.replay()
+        step_graph.replay()
         torch.cuda.synchronize()
-    for _ in range(args.warmup):
+    for _ in range(max(3, args.warmup)):
         step_graph.replay()
     torch.cuda.synchronize()
     st, where, block = qlin.device_error_detail()
     if st != qlin.QLIN_OK:
-        raise SystemExit(f"device status after warm-up: {qlin.status_string(st)} "
+        raise SystemExit(f"{name}: device status after warm-up: {qlin.status_string(st)} "
                          f"(wait {where}, block {block})")
-
-    clocks = ClockSampler(local_rank)
-    if dist:
+    if steps is None:
+        # sub-records: about a quarter of a second of timed replays
+        one = time_graph(torch, step_graph, 1)
+        steps = int(min(1000, max(5, round(0.25 / max(one, 1e-6)))))
+    reps = steps           # graph replays; each replay runs `copies` steps
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    t_step = time_graph(torch, step_graph, args.steps)
-    t_gemm = time_graph(torch, gemm_graph, args.steps)
-    t_alt = time_graph(torch, alt_graph, args.steps) if alt_graph is not None else 0.0
-    clock_info = clocks.stop()
+    t_step = time_graph(torch, step_graph, reps)
+    t_gemm = time_graph(torch, gemm_graph, reps)
+    t_alt = time_graph(torch, alt_graph, reps) if alt_graph is not None else 0.0
+    clock_info = clocks.stop() if clocks is not None else None
     t_step, t_gemm, t_alt = max_over_ranks([t_step, t_gemm, t_alt], device)
+    n_steps = reps * copies
 
     # End to end through the binding, no graph: every step copies its inputs
     # from pinned host memory and reads its outputs back.  Two sets of device
@@ -454,18 +529,18 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(v.numel() * 2 for v in host_in.values())
     d2h = sum(y.numel() * y.element_size() for y in runner.outputs(fused, 0))
     comp = torch.cuda.current_stream()
-    copy = torch.cuda.Stream(device)
+    copy_s = torch.cuda.Stream(device)
     in_ready = [torch.cuda.Event() for _ in range(2)]
     out_read = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
 
     def upload(b):
         # the inputs of set b were last read by the step that computed on b
-        copy.wait_event(comp_done[b])
-        with torch.cuda.stream(copy):
+        copy_s.wait_event(comp_done[b])
+        with torch.cuda.stream(copy_s):
             for k, v in host_in.items():
                 in_sets[b][k].copy_(v, non_blocking=True)
-        in_ready[b].record(copy)
+        in_ready[b].record(copy_s)
 
     def run_steps(n):
         upload(0)
@@ -474,96 +549,93 @@ def run_ours(args, rank, world, local_rank):
             comp.wait_event(in_ready[b])
             comp.wait_event(out_read[b])      # outputs of set b read back
             runner.inputs = in_sets[b]
-            runner.step(fused, b)
+            runner.step(fused, b, i % copies)
             comp_done[b].record(comp)
             if i + 1 < n:
                 upload(b ^ 1)
-            copy.wait_event(comp_done[b])
-            with torch.cuda.stream(copy):
-                for h, y in zip(host_out[b], runner.outputs(fused, b)):
+            copy_s.wait_event(comp_done[b])
+            with torch.cuda.stream(copy_s):
+                for h, y in zip(host_out[b], runner.outputs(fused, b, i % copies)):
                     h.copy_(y, non_blocking=True)
-            out_read[b].record(copy)
+            out_read[b].record(copy_s)
         torch.cuda.synchronize()
         runner.inputs = inputs0
 
     run_steps(max(2, args.warmup))
-    e2e_reps = max(3, min(args.steps, 100))
+    e2e_steps = max(3 * copies, min(n_steps, 100))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    run_steps(e2e_reps)
-    t_e2e = (time.perf_counter() - t0) / e2e_reps
+    run_steps(e2e_steps)
+    t_e2e = (time.perf_counter() - t0) / e2e_steps
     t_e2e, = max_over_ranks([t_e2e], device)
     st, where, block = qlin.device_error_detail()
     if st != qlin.QLIN_OK:
-        raise SystemExit(f"device status after timing: {qlin.status_string(st)} "
+        raise SystemExit(f"{name}: device status after timing: {qlin.status_string(st)} "
                          f"(wait {where}, block {block})")
 
-    if rank != 0:
-        return None
-    ms = t_step / args.steps * 1e3
-    value = whole_job_rate(runner.weight_bytes, args.steps, world, t_step) / 1e9
-    hbm, bf16, peak_src = measured_peaks()
-    gemm_avg_s = t_gemm / (args.steps * runner.n_gemm(fused))
-    bytes_per_launch = runner.gemm_bytes(fused) / runner.n_gemm(fused)
-    achieved = bytes_per_launch / gemm_avg_s / 1e9
-    line = {
-        "metric": "W8A8-GS128 linear weight GB/s (TOPS beside it); % of HBM roofline",
-        "value": round(value, 2),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "int8xint8->fp32 (exact on fp16 tcgen05), bf16 out",
-        "data": "synthetic (seeded splitmix64; weights uniform int8, fp16 log-uniform scales)",
-        "config": {
-            "workload": WORKLOAD_DESC[args.workload],
-            "linears_per_step": len(runner.specs),
-            "gemm_launches_per_step": runner.n_gemm(fused),
-            "fused_projections": ("projections that read the same input (q/k/v, gate/up) run as one "
-                                  "GEMM over their weights concatenated along N: same bytes and outputs"
-                                  if fused else "off: one GEMM per linear"),
-            "act_quant_per_step": runner.n_actq,
-            "weight_bytes_per_step": runner.weight_bytes,
-            "tops": round(runner.ops * args.steps * world / t_step / 1e12, 3),
-            "l2": "inputs larger than L2: each step streams its weight bytes once; "
-                  "no matrix is re-read before the others have passed through",
-            "timing": f"CUDA graph of one step, CUDA events on the replay stream; {args.soak}s "
-                      "untimed soak before the warm-up steps",
-            "parallelism": f"replicas x{world}",
-        },
-        "gpu_launches": runner.n_launches(fused) * args.steps,
-        "roofline": {
-            "bound": "hbm",
-            "kernel": "qlin_gemm_kernel (W8A8 GS128)",
-            "achieved": round(achieved, 1),
-            "peak": hbm,
-            "peak_source": peak_src,
-            "unit": "GB/s",
-            "frac": round(achieved / hbm, 4),
-            "traffic": profiled_traffic(args.workload, fused),
-            "bytes_per_launch": round(bytes_per_launch),
-            "avg_launch_us": round(gemm_avg_s * 1e6, 3),
-        },
-        "e2e": {
-            "value": round(runner.weight_bytes * world / t_e2e / 1e9, 2),
-            "unit": "GB/s",
-            "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(t_e2e * 1e3, 4),
-        },
+    peaks = measured_peaks()
+    n_gemm_launch = sum(1 for c in runner.calls[fused][0] if sel is None or sel(c))
+    gemm_avg_s = t_gemm / (reps * copies * n_gemm_launch)
+    gbs = whole_job_rate(runner.weight_bytes, n_steps, world, t_step) / 1e9
+    tops = whole_job_rate(runner.ops, n_steps, world, t_step) / 1e12
+    if bound_of(name) == "tensor":
+        ops_per_launch = runner.gemm_ops(fused, sel) / n_gemm_launch
+        achieved = ops_per_launch / gemm_avg_s / 1e12
+        roof = {"bound": "tensor", "kernel": "qlin_gemm_kernel (W8A8 GS128), M >= %d" % LARGE_M,
+                "achieved": round(achieved, 1), "peak": peaks["bf16_sustained"],
+                "peak_source": peaks["source"] + " (bf16 sustained: launches inside a long step)",
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_sustained"], 4),
+                "frac_of_burst_peak": round(achieved / peaks["bf16"], 4),
+                "traffic": profiled_traffic(name),
+                "ops_per_launch": round(ops_per_launch), "avg_launch_us": round(gemm_avg_s * 1e6, 3)}
+        value, unit = tops, "TOPS"
+    else:
+        bytes_per_launch = runner.gemm_bytes(fused) / n_gemm_launch
+        achieved = bytes_per_launch / gemm_avg_s / 1e9
+        roof = {"bound": "hbm", "kernel": "qlin_gemm_kernel (%s)" % (
+                    "W4A16 g128" if name == "w4a16" else "W8A16" if name == "w8a16" else "W8A8 GS128"),
+                "achieved": round(achieved, 1), "peak": peaks["hbm"],
+                "peak_source": peaks["source"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm"], 4),
+                "traffic": profiled_traffic(name),
+                "bytes_per_launch": round(bytes_per_launch),
+                "avg_launch_us": round(gemm_avg_s * 1e6, 3)}
+        value, unit = gbs, "GB/s"
+    e2e_gbs = runner.weight_bytes * world / t_e2e / 1e9
+    e2e_tops = runner.ops * world / t_e2e / 1e12
+    rec = {
+        "value": round(value, 3 if unit == "TOPS" else 2),
+        "unit": unit,
+        "steps": n_steps,
+        "ms_per_step": round(t_step / n_steps * 1e3, 4),
+        "gbs": round(gbs, 2),
+        "tops": round(tops, 3),
+        "config": workload_config(name, fused, world),
+        "gemm_launches_per_step": runner.n_gemm(fused),
+        "act_quant_per_step": runner.n_actq,
+        "gpu_launches": runner.n_launches(fused) * n_steps,
+        "l2": ("inputs larger than L2: each step streams its weight bytes once; no matrix is "
+               "re-read before the others have passed through" if copies == 1 else
+               f"weights smaller than L2: {copies} distinct copies of the weights "
+               f"({copies * runner.weight_bytes / 1e6:.0f} MB), used in turn by consecutive steps"),
+        "timing": (f"CUDA graph of {copies} step(s), {reps} replays timed with CUDA events on the "
+                   f"replay stream after {max(3, args.warmup)} warm-up replays"),
+        "roofline": roof,
+        "e2e": {"value": round(e2e_tops if unit == "TOPS" else e2e_gbs, 3 if unit == "TOPS" else 2),
+                "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(t_e2e * 1e3, 4)},
         "clocks": clock_info,
-        "other_call_list": (None if alt_graph is None else {
-            "fused_projections": not fused,
-            "value": round(runner.weight_bytes * args.steps * world / t_alt / 1e9, 2),
-            "unit": "GB/s",
-            "ms_per_step": round(t_alt / args.steps * 1e3, 4),
-            "gemm_launches_per_step": runner.n_gemm(not fused)}),
     }
-    return line, runner
+    if alt_graph is not None:
+        alt_gbs = whole_job_rate(runner.weight_bytes, n_steps, world, t_alt) / 1e9
+        alt_tops = whole_job_rate(runner.ops, n_steps, world, t_alt) / 1e12
+        rec["other_call_list"] = {
+            "fused_projections": not fused,
+            "value": round(alt_tops, 3) if unit == "TOPS" else round(alt_gbs, 2),
+            "unit": unit, "gbs": round(alt_gbs, 2), "tops": round(alt_tops, 3),
+            "ms_per_step": round(t_alt / n_steps * 1e3, 4),
+            "gemm_launches_per_step": runner.n_gemm(not fused)}
+    return rec, runner
 
 
 # ------------------------------------------- fused producers (RMSNorm, SiLU*up)
@@ -610,25 +682,6 @@ def _make_producer_inputs(kind, M, K, seed):
         return np.ascontiguousarray(np.tile(x, (reps, 1))[:M]), g
     x = synth.activations(seed, f"producers/silu/M{M}", r, 2 * K, "normal2")
     return np.ascontiguousarray(np.tile(x, (reps, 1))[:M]), None
-
-
-def profiled_producer_traffic():
-    """DRAM bytes of the dominant producer launch from the committed ncu
-    summary, or None when act_quant.cu changed since that capture."""
-    import hashlib
-    with open(os.path.join(ROOT, "w4a16_linear_layers_gb300", "csrc", "act_quant.cu"), "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    try:
-        with open(os.path.join(ROOT, "profiles", "producers_rmsnorm_silu_quant.md")) as f:
-            text = f.read()
-    except OSError:
-        return None
-    if h not in text:
-        return None
-    for line in text.splitlines():
-        if line.startswith("traffic_bytes_per_launch_top:"):
-            return int(line.split(":")[1])
-    return None
 
 
 def run_producers(args, rank, world, local_rank):
@@ -723,7 +776,8 @@ def run_producers(args, rank, world, local_rank):
         return None
     step_bytes = sum(producer_bytes(k, M, K) for k, M, K in specs)
     top_bytes = producer_bytes(top[0], top[1], top[2])
-    hbm, _, peak_src = measured_peaks()
+    peaks = measured_peaks()
+    hbm, peak_src = peaks["hbm"], peaks["source"]
     top_s = t_top / args.steps
     achieved = top_bytes / top_s / 1e9
     return {
@@ -758,7 +812,7 @@ def run_producers(args, rank, world, local_rank):
             "peak_source": peak_src,
             "unit": "GB/s",
             "frac": round(achieved / hbm, 4),
-            "traffic": profiled_producer_traffic(),
+            "traffic": profiled_traffic("producers", ("act_quant.cu",)),
             "bytes_per_launch": top_bytes,
             "avg_launch_us": round(top_s * 1e6, 3),
         },
@@ -826,8 +880,10 @@ def oracle_sample(specs, budget_s, seed=0, cache=None, frac=None):
     """Time the oracle on a bounded sample of the workload: for every linear
     of the step, the same fraction of its output columns (all rows), run on
     all host cores (one thread per column slice; the C oracle runs without the
-    GIL).  The fraction is calibrated to the time budget unless given.
-    Returns (weight bytes covered, seconds, threads, description, fraction)."""
+    GIL).  The sampled columns' weights are drawn alone (the generator is
+    counter-based).  The fraction is calibrated to the time budget unless
+    given.  Returns (weight bytes covered, ops covered, seconds, threads,
+    description, fraction)."""
     from concurrent.futures import ThreadPoolExecutor
 
     import oracle
@@ -838,16 +894,20 @@ def oracle_sample(specs, budget_s, seed=0, cache=None, frac=None):
     cache = {} if cache is None else cache
 
     def operands(name, K, N, kind, M, wk, nc):
-        key = (name, wk)
-        if key not in cache:
-            if wk.startswith("w8a8"):
-                cache[key] = synth.w8a8_weights(seed, name, K, N)
-            elif wk == "w8a16":
-                cache[key] = synth.w8a16_weights(seed, name + "/w8a16", K, N, W8A16_GROUP)
-            else:
-                cache[key] = synth.w4a16_weights(seed, name + "/w4", K, N)
-        q, s = cache[key]
-        q, s = np.ascontiguousarray(q[:, :nc]), np.ascontiguousarray(s[:, :nc])
+        cols = np.arange(nc)
+        if wk.startswith("w8a8"):
+            q = synth.randint_at(seed, name + "/qw", N, np.arange(K), cols, -127, 127)
+            s = synth.f16_bits(synth.log_uniform_at(seed, name + "/sw", N, np.arange(K // 128),
+                                                    cols, 1e-3, 1e-2))
+        elif wk == "w8a16":
+            q = synth.randint_at(seed, name + "/w8a16/qw", N, np.arange(K), cols, -127, 127)
+            s = synth.bf16_bits(synth.log_uniform_at(seed, name + "/w8a16/sw", N,
+                                                     np.arange(K // W8A16_GROUP), cols, 1e-3, 1e-2))
+        else:
+            q = synth.randint_at(seed, name + "/w4/qw", N, np.arange(K), cols, -7, 7)
+            s = synth.bf16_bits(synth.log_uniform_at(seed, name + "/w4/sw", N, np.arange(K // 128),
+                                                     cols, 1e-3, 3e-2))
+        q, s = np.ascontiguousarray(q), np.ascontiguousarray(s)
         xb = synth.activations(seed, f"{synth.shared_input_name(name)}/M{M}", M, K, kind)
         if wk.startswith("w8a8"):
             qw, _, _ = oracle.pack_gptq(q, 8)
@@ -860,14 +920,15 @@ def oracle_sample(specs, budget_s, seed=0, cache=None, frac=None):
         return (lambda ch, a=(xb, qw, s, K): oracle.gemm_w4a16_g128(*a, cols=ch))
 
     def run(frac):
-        total_bytes = 0
+        total_bytes, total_ops = 0, 0
         tasks = []
         for name, K, N, kind, M, wk in specs:
             nc = max(1, int(round(N * frac)))
             total_bytes += weight_bytes(K, nc, wk)
+            total_ops += 2 * M * K * nc
             key = ("operands", name, K, N, kind, M, wk, nc)
             if key not in cache:
-                cache[key] = operands(name, K, N, kind, M, wk, nc)
+                cache[key] = operands(name, K, N, kind, M, wk.replace("_argmax", ""), nc)
             fn = cache[key]
             for ch in np.array_split(np.arange(nc), min(nthreads, nc)):
                 if ch.size:
@@ -875,20 +936,29 @@ def oracle_sample(specs, budget_s, seed=0, cache=None, frac=None):
         t0 = time.perf_counter()
         with ThreadPoolExecutor(nthreads) as ex:
             list(ex.map(lambda t: t[0](t[1]), tasks))
-        return total_bytes, time.perf_counter() - t0
+        return total_bytes, total_ops, time.perf_counter() - t0
 
     if frac is None:
-        frac = 0.001
+        frac = 1e-4
         while True:                       # calibrate the sample size on this host
-            _, t = run(frac)
+            _, _, t = run(frac)
             if t >= 0.2 * budget_s or frac >= 1.0:
                 break
             frac = min(1.0, frac * min(16.0, max(2.0, 0.3 * budget_s / max(t, 1e-3))))
         frac = min(1.0, frac * budget_s / max(t, 1e-3))
-    b, t = run(frac)
+    b, ops, t = run(frac)
     desc = (f"oracle on {frac * 100:.3f}% of the output columns of every linear of the step "
             f"(all rows), {nthreads} threads")
-    return b, t, nthreads, desc, frac
+    return b, ops, t, nthreads, desc, frac
+
+
+def cpu_baseline_record(name, specs, budget_s):
+    b, ops, t, thr, desc, _ = oracle_sample(specs, budget_s)
+    if bound_of(name) == "tensor":
+        return {"value": round(ops / t / 1e12, 6), "unit": "TOPS", "cores": thr, "kind": "oracle",
+                "sample": desc}
+    return {"value": round(b / t / 1e9, 6), "unit": "GB/s", "cores": thr, "kind": "oracle",
+            "sample": desc}
 
 
 def run_reference_producers(args):
@@ -930,26 +1000,31 @@ def run_reference(args, rank, world):
         return None
     if args.workload == "producers":
         return run_reference_producers(args)
-    specs = workload_specs(args.workload)
+    name = HEADLINE if args.workload == "all" else args.workload
+    specs = workload_specs(name)
     # about a minute of oracle work over all warm-up and timed steps: the
     # sample fraction is calibrated once, then every step runs that sample
     per_step_budget = max(0.02, 60.0 / max(1, args.steps + args.warmup))
     cache = {}
-    _, _, _, _, frac = oracle_sample(specs, per_step_budget, cache=cache)
+    frac = oracle_sample(specs, per_step_budget, cache=cache)[5]
     for _ in range(args.warmup):
         oracle_sample(specs, per_step_budget, cache=cache, frac=frac)
-    tot_b, tot_t = 0, 0.0
+    tot_b, tot_ops, tot_t = 0, 0, 0.0
     desc, thr = "", 1
     for _ in range(args.steps):
-        b, t, thr, desc, _ = oracle_sample(specs, per_step_budget, cache=cache, frac=frac)
+        b, ops, t, thr, desc, _ = oracle_sample(specs, per_step_budget, cache=cache, frac=frac)
         tot_b += b
+        tot_ops += ops
         tot_t += t
-    value = tot_b / tot_t / 1e9
+    if bound_of(name) == "tensor":
+        value, unit = tot_ops / tot_t / 1e12, "TOPS"
+    else:
+        value, unit = tot_b / tot_t / 1e9, "GB/s"
     return {
         "impl": "reference",
-        "metric": "W8A8-GS128 linear weight GB/s (TOPS beside it); % of HBM roofline",
+        "metric": METRIC,
         "value": round(value, 6),
-        "unit": "GB/s",
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -959,10 +1034,10 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "int8xint8->int64 exact, fp32 rescale chain (CPU oracle)",
         "data": "synthetic (seeded splitmix64)",
-        "config": {"workload": WORKLOAD_DESC[args.workload]},
-        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": thr,
+        "config": workload_config(name, not args.no_fuse, world),
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": thr,
                          "kind": "oracle", "sample": desc},
-        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
 
@@ -972,16 +1047,19 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--soak", type=float, default=0.5,
                     help="seconds of untimed replays before the warm-up (clock ramp)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="layer", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--workload", default="all", choices=["all"] + sorted(WORKLOAD_DESC),
+                    help="all: the headline drafter layer plus every other configuration as "
+                         "sub-records")
     ap.add_argument("--no-fuse", action="store_true",
                     help="one GEMM per linear (default: projections sharing an input run as one GEMM)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
-                    help="seconds of oracle work for the cpu_baseline sample")
+                    help="seconds of oracle work for the headline's cpu_baseline sample "
+                         "(a third of it for each sub-record)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -994,12 +1072,18 @@ def main():
         if line is not None:
             print(json.dumps(line), flush=True)
         return
+    import torch
+
     if world > 1:
-        import torch
         import torch.distributed as dist
 
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
+    from w4a16_linear_layers_gb300 import build as qbuild
+
+    qbuild.build()
+    device = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(device)
     if args.workload == "producers":
         line = run_producers(args, rank, world, local_rank)
         if line is not None:
@@ -1007,15 +1091,57 @@ def main():
             line["cpu_baseline"] = {"value": round(b / t / 1e9, 6), "unit": "GB/s", "cores": thr,
                                     "kind": "oracle", "sample": desc}
             print(json.dumps(line), flush=True)
-        out = None
     else:
-        out = run_ours(args, rank, world, local_rank)
-    if out is not None:
-        line, runner = out
-        b, t, thr, desc, _ = oracle_sample(runner.specs, args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(b / t / 1e9, 6), "unit": "GB/s", "cores": thr,
-                                "kind": "oracle", "sample": desc}
-        print(json.dumps(line), flush=True)
+        fused = not args.no_fuse
+        name = HEADLINE if args.workload == "all" else args.workload
+        clocks = ClockSampler(local_rank)
+        rec, runner = measure(name, args, device, world, args.steps, fused, with_alt=True,
+                              clocks=clocks)
+        specs = runner.specs
+        del runner
+        subs = {}
+        if args.workload == "all":
+            for sub in SUB_RECORDS:
+                torch.cuda.empty_cache()
+                r, sub_runner = measure(sub, args, device, world, None, fused)
+                subs[sub] = (r, sub_runner.specs)
+                del sub_runner
+        if rank == 0:
+            line = {
+                "metric": METRIC,
+                "value": rec["value"],
+                "unit": rec["unit"],
+                "n_gpus": world,
+                "steps": rec["steps"],
+                "warmup": args.warmup,
+                "ms_per_step": rec["ms_per_step"],
+                "higher_is_better": True,
+                "scaling": "weak",
+                "vs_baseline": None,
+                "dtype": "int8xint8->fp32 (exact on fp16 tcgen05), bf16 out"
+                         if name not in ("w4a16", "w8a16") else "bf16 x int weights -> fp32, bf16 out",
+                "data": "synthetic (seeded splitmix64; weights uniform int8/int4, log-uniform "
+                        "group scales; activations N(0,1) with outlier channels)",
+                "config": rec["config"],
+                "tops": rec["tops"],
+                "gemm_launches_per_step": rec["gemm_launches_per_step"],
+                "act_quant_per_step": rec["act_quant_per_step"],
+                "l2": rec["l2"],
+                "timing": rec["timing"],
+                "gpu_launches": rec["gpu_launches"],
+                "roofline": rec["roofline"],
+                "e2e": rec["e2e"],
+                "clocks": rec["clocks"],
+            }
+            if "other_call_list" in rec:
+                line["other_call_list"] = rec["other_call_list"]
+            line["cpu_baseline"] = cpu_baseline_record(name, specs, args.cpu_budget)
+            if subs:
+                line["configs"] = {}
+                for sub, (r, sub_specs) in subs.items():
+                    r["cpu_baseline"] = cpu_baseline_record(sub, sub_specs, args.cpu_budget / 3)
+                    line["configs"][sub] = r
+            print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
 

@@ -130,6 +130,64 @@ def log_uniform(seed: int, name: str, shape, lo: float, hi: float) -> np.ndarray
     return np.exp(np.log(lo) + u * (np.log(hi) - np.log(lo)))
 
 
+def randint_at(seed: int, name: str, ncols: int, rows, cols, lo: int, hi: int,
+               dtype=np.int8) -> np.ndarray:
+    """The entries [rows][:, cols] of randint(seed, name, (R, ncols), lo, hi):
+    element (r, c) is word r * ncols + c of the stream, so a sub-grid costs
+    only its own words."""
+    base = _base(seed, name)
+    r = np.asarray(rows, np.uint64)[:, None]
+    c = np.asarray(cols, np.uint64)[None, :]
+    idx = r * np.uint64(ncols) + c + np.uint64(1)
+    with np.errstate(over="ignore"):
+        w = _mix64(base + idx * _GOLDEN)
+    return (((w >> np.uint64(11)) % np.uint64(hi - lo + 1)).astype(np.int64) + lo).astype(dtype)
+
+
+def log_uniform_at(seed: int, name: str, ncols: int, rows, cols, lo: float, hi: float) -> np.ndarray:
+    """The entries [rows][:, cols] of log_uniform(seed, name, (R, ncols), lo, hi)."""
+    base = _base(seed, name)
+    r = np.asarray(rows, np.uint64)[:, None]
+    c = np.asarray(cols, np.uint64)[None, :]
+    idx = r * np.uint64(ncols) + c + np.uint64(1)
+    with np.errstate(over="ignore"):
+        w = _mix64(base + idx * _GOLDEN)
+    u = ((w >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0**-53
+    return np.exp(np.log(lo) + u * (np.log(hi) - np.log(lo)))
+
+
+def randint_device(seed: int, name: str, shape, lo: int, hi: int, device):
+    """randint(seed, name, shape, lo, hi, int8) drawn by torch on `device`,
+    bit for bit the same integers (the words are formed in int64 with
+    two's-complement wraparound, and logical shifts are arithmetic shifts
+    masked to the unsigned width).  Used for weight matrices of gigabytes,
+    which the numpy path would take minutes to draw."""
+    import torch
+
+    def s64(v):                      # uint64 constant -> the int64 with its bits
+        return v - (1 << 64) if v >= (1 << 63) else v
+
+    def shr(z, k):
+        return (z >> k) & ((1 << (64 - k)) - 1)
+
+    golden, m1, m2 = s64(int(_GOLDEN)), s64(int(_M1)), s64(int(_M2))
+    base = s64(int(_base(seed, name)))
+    n = _count(shape)
+    out = torch.empty(n, dtype=torch.int8, device=device)
+    step = 1 << 25
+    for s in range(0, n, step):
+        c = min(step, n - s)
+        z = torch.arange(s + 1, s + c + 1, dtype=torch.int64, device=device)
+        z = z * golden + base
+        z = z ^ shr(z, 30)
+        z = z * m1
+        z = z ^ shr(z, 27)
+        z = z * m2
+        z = z ^ shr(z, 31)
+        out[s:s + c] = (torch.remainder(shr(z, 11), hi - lo + 1) + lo).to(torch.int8)
+    return out.view(*shape)
+
+
 def choice_without_replacement(seed: int, name: str, n: int, k: int) -> np.ndarray:
     """k distinct indices of range(n): the k smallest of n random keys."""
     keys = _words(_base(seed, name), 0, n)
