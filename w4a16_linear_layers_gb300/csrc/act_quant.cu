@@ -149,20 +149,6 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
 // store it, and quantized exactly as act_quant_kernel does; it is also
 // written out when y is not null.
 
-// Sum over the block (every thread gets the result).  `red` is reused by the
-// next reduction only after the barrier at the start of the next call.
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = red[0];
-#pragma unroll
-  for (int w = 1; w < kAqThreads / 32; ++w) t += red[w];
-  return t;
-}
-
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -175,40 +161,113 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return t;
 }
 
-__device__ __forceinline__ float sumsq8(uint4 v, float acc) {
+// ---- exact producer outputs
+//
+// The producers' bf16 outputs are the oracle's: each value is first formed in
+// fp32, and where that fp32 value lies so close to a point halfway between
+// two bf16 values that its known error could put the exact value on the other
+// side, the value is formed again in fp64 and rounded from there.
+
+// v added into the unevaluated sum s + c without rounding error in the
+// transformation (Knuth's TwoSum); c collects what each addition dropped.
+__device__ __forceinline__ void df_add(float& s, float& c, float v) {
+  const float t = __fadd_rn(s, v);
+  const float bp = __fsub_rn(t, s);
+  const float ap = __fsub_rn(t, bp);
+  c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, ap), __fsub_rn(v, bp)));
+  s = t;
+}
+
+// Squares of 8 bf16 values (each exact in fp32: 8 significant bits squared)
+// added into s + c.
+__device__ __forceinline__ void sumsq8(uint4 v, float& s, float& c) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    acc = __fmaf_rn(bf16_lo(w[i]), bf16_lo(w[i]), acc);
-    acc = __fmaf_rn(bf16_hi(w[i]), bf16_hi(w[i]), acc);
+    df_add(s, c, __fmul_rn(bf16_lo(w[i]), bf16_lo(w[i])));
+    df_add(s, c, __fmul_rn(bf16_hi(w[i]), bf16_hi(w[i])));
   }
-  return acc;
 }
 
-// RMSNorm output of 8 elements: t = bf16(x * rstd), z = bf16(gamma * t)
-// (the product of two bf16 values is exact in fp32, so z is rounded once).
-__device__ __forceinline__ uint32_t norm2(uint32_t x, uint32_t g, float rstd) {
-  const uint32_t t = bf16x2_rn(__fmul_rn(bf16_lo(x), rstd), __fmul_rn(bf16_hi(x), rstd));
-  return bf16x2_rn(__fmul_rn(bf16_lo(g), bf16_lo(t)), __fmul_rn(bf16_hi(g), bf16_hi(t)));
+// True when the fp32 value with bits u is within k fp32 ulps of a point
+// halfway between two bf16 values (low 16 bits 0x8000), in either direction.
+__device__ __forceinline__ bool near_bf16_half(uint32_t u, uint32_t k) {
+  return ((u & 0xFFFFu) - (0x8000u - k)) <= 2u * k;
 }
 
-__device__ __forceinline__ uint4 norm8(uint4 x, uint4 g, float rstd) {
-  return make_uint4(norm2(x.x, g.x, rstd), norm2(x.y, g.y, rstd), norm2(x.z, g.z, rstd),
-                    norm2(x.w, g.w, rstd));
+__device__ __forceinline__ uint32_t bf16_bits_rn(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// SiLU(g) * u of 8 elements in fp32, rounded once to bf16: SiLU(g) =
-// g * sigmoid(g), the sigmoid from e = exp(-|g|) <= 1 (1 / (1 + e) for g >= 0,
-// e / (1 + e) below), so the divisor stays in [1, 2] and the approximate
-// divide (within 2 ulp there) never meets an overflowing exponential.
-__device__ __forceinline__ float silu_mul1(float g, float u) {
+// bf16 bits of a binary64 value rounded once to nearest even: through the
+// nearest fp32 value f, which rounds to the same bf16 value unless f is
+// itself a halfway point; then the fp64 value picks the side.
+__device__ __forceinline__ uint32_t f64_to_bf16_bits(double d) {
+  const float f = __double2float_rn(d);
+  const uint32_t u = __float_as_uint(f);
+  if ((u & 0xFFFFu) == 0x8000u) {
+    const double back = static_cast<double>(f);
+    if (d != back) return fabs(d) > fabs(back) ? ((u >> 16) + 1u) & 0xFFFFu : (u >> 16);
+  }
+  return bf16_bits_rn(f);
+}
+
+// The norm's scale 1 / sqrt(ss / K + eps), formed once per row in fp64 from
+// the compensated sum of squares; rhi is its nearest fp32 value.
+struct RowScale {
+  double rstd;
+  float rhi;
+};
+
+__device__ __forceinline__ RowScale row_scale(double ss, int64_t K, float eps) {
+  const double r = 1.0 / sqrt(ss / static_cast<double>(K) + static_cast<double>(eps));
+  return RowScale{r, __double2float_rn(r)};
+}
+
+// t = bf16(x * rstd).  x * rhi in fp32 is within 2 fp32 ulps of x * rstd (rhi
+// and the product each rounded once), so its bf16 rounding is the exact
+// one unless it lies within 4 ulps of a halfway point; those are formed in
+// fp64.
+__device__ __forceinline__ float norm_t(float x, const RowScale& rs) {
+  const float t = __fmul_rn(x, rs.rhi);
+  const uint32_t b = near_bf16_half(__float_as_uint(t), 4u)
+                         ? f64_to_bf16_bits(static_cast<double>(x) * rs.rstd)
+                         : bf16_bits_rn(t);
+  return __uint_as_float(b << 16);
+}
+
+// RMSNorm output of 2 elements: t = bf16(x * rstd), z = bf16(gamma * t) (the
+// product of two bf16 values is exact in fp32, so z is rounded once).
+__device__ __forceinline__ uint32_t norm2(uint32_t x, uint32_t g, const RowScale& rs) {
+  return bf16x2_rn(__fmul_rn(bf16_lo(g), norm_t(bf16_lo(x), rs)),
+                   __fmul_rn(bf16_hi(g), norm_t(bf16_hi(x), rs)));
+}
+
+__device__ __forceinline__ uint4 norm8(uint4 x, uint4 g, const RowScale& rs) {
+  return make_uint4(norm2(x.x, g.x, rs), norm2(x.y, g.y, rs), norm2(x.z, g.z, rs),
+                    norm2(x.w, g.w, rs));
+}
+
+// bf16(SiLU(g) * u).  In fp32: SiLU(g) = g * sigmoid(g), the sigmoid from
+// e = exp(-|g|) <= 1 (1 / (1 + e) for g >= 0, e / (1 + e) below), so the
+// divisor stays in [1, 2] and no exponential overflows.  With expf within 2
+// ulps and the approximate divide within 2 ulps on that range (the CUDA
+// programming guide's maximum-error tables), plus four roundings, the fp32
+// value is within 12 ulps of the exact one; within 16 ulps of a bf16 halfway
+// point it is formed again in fp64 as g / (1 + exp(-g)) * u.
+__device__ __forceinline__ uint32_t silu_mul1(float g, float u) {
   const float e = expf(-fabsf(g));
   const float sig = __fdividef(g >= 0.0f ? 1.0f : e, __fadd_rn(1.0f, e));
-  return __fmul_rn(__fmul_rn(g, sig), u);
+  const float v = __fmul_rn(__fmul_rn(g, sig), u);
+  if (near_bf16_half(__float_as_uint(v), 16u)) {
+    const double gd = static_cast<double>(g);
+    return f64_to_bf16_bits(gd / (1.0 + exp(-gd)) * static_cast<double>(u));
+  }
+  return bf16_bits_rn(v);
 }
 
 __device__ __forceinline__ uint32_t silu_mul2(uint32_t g, uint32_t u) {
-  return bf16x2_rn(silu_mul1(bf16_lo(g), bf16_lo(u)), silu_mul1(bf16_hi(g), bf16_hi(u)));
+  return silu_mul1(bf16_lo(g), bf16_lo(u)) | (silu_mul1(bf16_hi(g), bf16_hi(u)) << 16);
 }
 
 __device__ __forceinline__ uint4 silu_mul8(uint4 g, uint4 u) {
@@ -216,15 +275,44 @@ __device__ __forceinline__ uint4 silu_mul8(uint4 g, uint4 u) {
                     silu_mul2(g.w, u.w));
 }
 
+// Sum of the pairs (s, c) over the block, in fp64, formed by thread 0 alone
+// (fp64 arithmetic is slow on this part) and returned to every thread through
+// shared memory: pairs are combined across each warp with TwoSum, then
+// thread 0 adds the warps' pairs in fp64.
+template <int kThreads>
+__device__ __forceinline__ RowScale block_row_scale(float s, float c, float2* red2,
+                                                    RowScale* shared_rs, int64_t K, float eps) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    const float c2 = __shfl_xor_sync(0xFFFFFFFFu, c, o);
+    df_add(s, c, s2);
+    c = __fadd_rn(c, c2);
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red2[threadIdx.x >> 5] = make_float2(s, c);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double ss = 0.0;
+#pragma unroll 1
+    for (int w = 0; w < kThreads / 32; ++w)
+      ss += static_cast<double>(red2[w].x) + static_cast<double>(red2[w].y);
+    *shared_rs = row_scale(ss, K, eps);
+  }
+  __syncthreads();
+  return *shared_rs;
+}
+
 // Rows longer than the persistent form holds (more than 32768 elements): one
 // block per row, the row read from memory on each pass (the second and third
-// from L2).  The norm: variance (fp32, per-thread fma chains then the block
-// sum), rstd = 1 / sqrt(variance + eps) with IEEE square root and divide, z,
-// then act-quant of z.
+// from L2).  The norm: the compensated sum of squares, rstd in fp64 (once per
+// row), z, then act-quant of z.
 __global__ void __launch_bounds__(kAqThreads) rmsnorm_quant_long_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps, int64_t K,
     int8_t* __restrict__ q, float* __restrict__ s_out, uint16_t* __restrict__ y) {
   __shared__ float red[kAqThreads / 32];
+  __shared__ float2 red2[kAqThreads / 32];
+  __shared__ RowScale row_rs;
   grid_dep_wait();
   grid_dep_launch();
   const int64_t m = blockIdx.x;
@@ -234,11 +322,9 @@ __global__ void __launch_bounds__(kAqThreads) rmsnorm_quant_long_kernel(
   uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
   uint4* yrow = y ? reinterpret_cast<uint4*>(y + m * K) : nullptr;
   const int tid = threadIdx.x;
-  float ss = 0.0f;
-  for (int64_t v = tid; v < nvec; v += kAqThreads) ss = sumsq8(__ldg(row + v), ss);
-  ss = block_sum(ss, red);
-  const float rstd =
-      __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps)));
+  float ss = 0.0f, sc = 0.0f;
+  for (int64_t v = tid; v < nvec; v += kAqThreads) sumsq8(__ldg(row + v), ss, sc);
+  const RowScale rstd = block_row_scale<kAqThreads>(ss, sc, red2, &row_rs, K, eps);
   float amax = 0.0f;
   for (int64_t v = tid; v < nvec; v += kAqThreads) {
     const uint4 z = norm8(__ldg(row + v), __ldg(grow + v), rstd);
@@ -309,19 +395,6 @@ struct ProducerParams {
 };
 
 template <int kThreads>
-__device__ __forceinline__ float block_sum_p(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = red[0];
-#pragma unroll
-  for (int w = 1; w < kThreads / 32; ++w) t += red[w];
-  return t;
-}
-
-template <int kThreads>
 __device__ __forceinline__ float block_max_p(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -339,6 +412,8 @@ __global__ void __launch_bounds__(kPThreads) producer_quant_kernel(const Produce
   extern __shared__ uint8_t psmem_raw[];
   __shared__ uint64_t full[kPMaxStages];
   __shared__ float red[kPThreads / 32];
+  __shared__ float2 red2[kPThreads / 32];
+  __shared__ RowScale row_rs;
   __shared__ int abort_flag;
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(psmem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -382,22 +457,22 @@ __global__ void __launch_bounds__(kPThreads) producer_quant_kernel(const Produce
     uint4 z[kPVec];
     float amax = 0.0f;
     if constexpr (kKind == kProdRms) {
-      float ss = 0.0f;
+      float ss = 0.0f, sc = 0.0f;
 #pragma unroll
       for (int j = 0; j < kPVec; ++j) {
         const int64_t v = tid + static_cast<int64_t>(j) * kPThreads;
         if (v < nvec) {
           z[j] = srow[v];
-          ss = sumsq8(z[j], ss);
+          sumsq8(z[j], ss, sc);
         }
       }
-      ss = block_sum_p<kPThreads>(ss, red);   // every thread has its part of the row in registers
+      // every thread has its part of the row in registers after the first
+      // barrier of the reduction
+      const RowScale rstd = block_row_scale<kPThreads>(ss, sc, red2, &row_rs, p.K, p.eps);
       if (tid == 0 && issued < nrows) {
         fence_proxy_async_smem();
         issue(issued++);
       }
-      const float rstd =
-          __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(p.K)), p.eps)));
 #pragma unroll
       for (int j = 0; j < kPVec; ++j) {
         const int64_t v = tid + static_cast<int64_t>(j) * kPThreads;
