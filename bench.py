@@ -375,9 +375,9 @@ class LayerRunner:
 
     def n_launches(self, fused):
         # one kernel per act-quant and per GEMM, plus the int8 -> fp16 operand
-        # pass of W8A8 GEMMs with token tiles of 96 (M > 64), plus the argmax
-        # decode
-        return self.n_actq + sum(1 + (c["wk"].startswith("w8a8") and c["M"] > 64)
+        # pass of W8A8 GEMMs with token tiles of 64 and more (M > 32), plus
+        # the argmax decode
+        return self.n_actq + sum(1 + (c["wk"].startswith("w8a8") and c["M"] > 32)
                                  + c["wk"].endswith("_argmax") for c in self.calls[fused][0])
 
     def _ikey(self, spec):

@@ -219,6 +219,51 @@ qlin_status_t qlin_gemm_w4a16_g128(const uint16_t *x, const int32_t *qweight,
                                    size_t workspace_bytes, qlin_stream_t stream);
 
 /*
+ * The weights in the tile layout: the same GPTQ words, reordered once (at
+ * load time) so that the GEMM's weight stream reads each step's tile as one
+ * contiguous block.  Tile (f, g) holds the words of output features
+ * 128f..128f+127 and K group g (K values 128g..128g+127): W x 128 int32, W =
+ * 32 words for 8-bit and 16 for 4-bit weights, word (kk, j) of the tile =
+ * qweight[g*W + kk][128f + j]; tiles follow each other by f, then g.  Words
+ * of features at or past N (the last tile, when N is not a multiple of 128)
+ * are 0 and never reach an output.
+ *
+ * Passages: "Qwen3.8-27B-DFlash2-W4A16-g128-sym-GPTQ" card, property table
+ * ("compressed-tensors pack-quantized (Marlin-compatible)": serving kernels
+ * take GPTQ words reordered for their own access pattern); the GPTQ format
+ * of the "Flint-DFlash2-GPTQ-INT8-PTQR" card.  The reordering is this
+ * library's own.
+ *
+ * qlin_tiles_bytes: bytes of the tile layout, ceil(N/128) * 128 * K * bits /
+ *   8; 0 for an invalid shape or bits.
+ * qlin_pack_tiles:
+ *   qweight  int32 [K*bits/32, N]  GPTQ words (device, 16-byte aligned)
+ *   bits     8 or 4
+ *   tiles    int32, qlin_tiles_bytes(K, N, bits) bytes (device, 16-byte
+ *            aligned, caller-owned)
+ *   Asynchronous on `stream`.  Errors: QLIN_ERR_NULL, QLIN_ERR_BITS,
+ *   QLIN_ERR_SHAPE (K a positive multiple of 128, N >= 1), QLIN_ERR_ALIGN.
+ *
+ * qlin_gemm_w8a8_gs128_tiled / qlin_gemm_w4a16_g128_tiled: the same linears
+ * as qlin_gemm_w8a8_gs128 / qlin_gemm_w4a16_g128, bit for bit, with the
+ * weights in the tile layout (`tiles`, from qlin_pack_tiles with bits 8 / 4)
+ * in place of qweight.  All other arguments, errors and the workspace are as
+ * for those calls.
+ */
+size_t qlin_tiles_bytes(int64_t K, int64_t N, int bits);
+qlin_status_t qlin_pack_tiles(const int32_t *qweight, int64_t K, int64_t N, int bits,
+                              int32_t *tiles, qlin_stream_t stream);
+qlin_status_t qlin_gemm_w8a8_gs128_tiled(const int8_t *q_a, const float *s_a,
+                                         const int32_t *tiles, const uint16_t *scales,
+                                         int64_t M, int64_t N, int64_t K, uint16_t *y,
+                                         void *workspace, size_t workspace_bytes,
+                                         qlin_stream_t stream);
+qlin_status_t qlin_gemm_w4a16_g128_tiled(const uint16_t *x, const int32_t *tiles,
+                                         const uint16_t *scales, int64_t M, int64_t N,
+                                         int64_t K, uint16_t *y, void *workspace,
+                                         size_t workspace_bytes, qlin_stream_t stream);
+
+/*
  * W8A16 int8 weight-only linear, bf16 activations:
  *   w[k,n] = bf16( q_w[k,n] * s[k / group_size, n] ),   y = bf16( sum_k x[m,k] * w[k,n] )
  * accumulated in fp32 (one rounding of each exact product q * s).
@@ -316,8 +361,8 @@ qlin_status_t qlin_ingest_nk(const int32_t *packed_nk, const uint16_t *scales_ng
 /*
  * Bytes of workspace the GEMMs need for (M, N, K) on the current device: a
  * fixed region of arrival counters (one per block), the fp32 split-K
- * partials of two output tiles per block, and, for token tiles of 96 and
- * more (M > 64), the fp16 image of the W8A8 activations.  Returns 0 for
+ * partials of two output tiles per block, and, for token tiles of 64 and
+ * more (M > 32), the fp16 image of the W8A8 activations.  Returns 0 for
  * shapes the GEMMs reject.
  */
 size_t qlin_workspace_bytes(int64_t M, int64_t N, int64_t K);
@@ -365,7 +410,9 @@ const char *qlin_status_string(qlin_status_t status);
  * GEMM, the greedy-argmax GEMMs, the compressed-tensors ingest, the fused
  * producers and qlin_device_error_detail to the 1.0 calls; no 1.0 call
  * changed, except that an empty batch (M == 0) now accepts NULL batch
- * buffers. */
+ * buffers.  1.2 (102) adds the tile layout (qlin_tiles_bytes,
+ * qlin_pack_tiles) and the tiled W8A8 and W4A16 GEMMs; the greedy-argmax
+ * calls now take at most 96 rows. */
 int qlin_version(void);
 
 #ifdef __cplusplus

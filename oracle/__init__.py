@@ -14,6 +14,7 @@ patterns):
 * ``unpack_gptq(qweight, K, N, bits)``-> q int8 [K,N]
 * ``group_partials_i8(qa, qweight, K)``-> P int32 [G,M,N]
 * ``gemm_w8a8_gs128(...)``            -> dict of y_bf16 / y_f32 / y64 / bound / abs_sum
+* ``pack_tiles(qweight, K, bits)``      -> the GEMMs' tile layout of the words
 * ``gemm_w4a16_g128(...)``            -> same dict
 * ``gemm_w8a16(..., group_size)``     -> same dict (int8 weight-only; g32, g128 or per channel)
 * ``dequant_w4a16(qweight, scales, K, N)`` -> w bf16 bits [K,N]
@@ -89,6 +90,8 @@ def _load():
             lib.orc_argmax_bf16_rows.restype = None
             lib.orc_ingest_nk.argtypes = [P, P, I, I, ctypes.c_int, P, P]
             lib.orc_ingest_nk.restype = None
+            lib.orc_pack_tiles.argtypes = [P, I, I, ctypes.c_int, P]
+            lib.orc_pack_tiles.restype = None
             lib.orc_gemm_w8a16.argtypes = [P, P, P, I, I, I, I, P, I, P, I, P, P, P, P, P]
             lib.orc_gemm_w8a16.restype = None
             lib.orc_f64_to_bf16.argtypes = [ctypes.c_double]
@@ -273,6 +276,17 @@ def ingest_nk(packed_nk, scales_ng_bits, K: int, N: int, bits: int):
     so = np.empty((K // 128, N), np.uint16)
     _load().orc_ingest_nk(_ptr(pk), _ptr(sc), K, N, bits, _ptr(qw), _ptr(so))
     return qw, so
+
+
+def pack_tiles(qweight, K: int, bits: int) -> np.ndarray:
+    """GPTQ words [K*bits/32, N] -> the flat int32 tile layout (tile (f, g) =
+    W x 128 words of features 128f.. and K group g, by f then g; 0 past N)."""
+    qw = _c(qweight, np.int32)
+    N = qw.shape[1]
+    F = (N + 127) // 128
+    out = np.empty(F * (K // 128) * (128 * bits // 32) * 128, np.int32)
+    _load().orc_pack_tiles(_ptr(qw), K, N, bits, _ptr(out))
+    return out
 
 
 # ------------------------------------------------------------ fused producers

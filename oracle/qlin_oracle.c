@@ -328,6 +328,25 @@ void orc_ingest_nk(const int32_t *packed_nk, const uint16_t *scales_ng, int64_t 
     }
 }
 
+/* The tile layout of the weights (a reordering of the GPTQ words, with no
+ * counterpart in the pages beyond the card's note that serving kernels take
+ * the words in their own, Marlin-compatible, order): tile (f, g) holds the
+ * words of output features 128f..128f+127 and K group g as W x 128 int32, W =
+ * 128 * bits / 32 words; word (kk, j) of the tile is GPTQ word (g*W + kk,
+ * 128f + j), or 0 past N; tiles follow each other by f, then g. */
+void orc_pack_tiles(const int32_t *qweight, int64_t K, int64_t N, int bits, int32_t *tiles)
+{
+    const int64_t W = GROUP * bits / 32, G = K / GROUP, F = (N + 127) / 128;
+    int64_t o = 0;
+    for (int64_t f = 0; f < F; ++f)
+        for (int64_t g = 0; g < G; ++g)
+            for (int64_t kk = 0; kk < W; ++kk)
+                for (int64_t j = 0; j < 128; ++j, ++o) {
+                    const int64_t n = 128 * f + j;
+                    tiles[o] = n < N ? qweight[(g * W + kk) * N + n] : 0;
+                }
+}
+
 /* W8A16 weight-only int8 linear ("Qwen3.5-4B-DFlash-W8A16" card: a
  * weight-only int8 drafter made by round-to-nearest on the weights; "DFlash2
  * decoding" recipe page: int8 drafter projections with group-32 scales).

@@ -2,7 +2,7 @@
 
 Each role of one block of `qlin_gemm_kernel` (the weight producer, the
 activation and scale producer, the two MMA issuers, the eight converter warps
-and the eight epilogue warps) is a generator that yields the kernel's
+and the epilogue warps) is a generator that yields the kernel's
 synchronisation actions in program order: waits on an mbarrier phase parity,
 arrivals, expect-tx arrivals, TMA loads (asynchronous, completing their
 transaction bytes later), MMAs (asynchronous) and `tcgen05.commit` (an
@@ -209,6 +209,9 @@ def _roles(c, st):
     WO, XC = c["mode"] == "wo", c["mode"] == "w8x"
     NB, ND, ST, NX = c["NB"], c["ND"], c["stages"], c["NX"]
     NXR = c.get("NXR", NX)
+    # A buffers freed by commits of their own (weight-only formats, and W8A8
+    # with fewer D buffers than A buffers); else by the step's D commit
+    ACOMMIT = WO or ND < NB
     n = len(st)
     pre = min(n, PRE_W, ST)
 
@@ -268,7 +271,7 @@ def _roles(c, st):
                 if not (WO and started):
                     yield ("wait", f"dempty{db}", dbph ^ 1)
                 yield ("mma", me, [f"A{ab}", f"X{j % NX}"])
-                if WO:
+                if ACOMMIT:
                     yield ("commit", me, f"aempty{ab}")
                 if not XC:
                     yield ("commit", me, f"xempty{j % NX}")
@@ -293,7 +296,7 @@ def _roles(c, st):
             if (j & 1) == grp:
                 ab, abph = j % NB, (j // NB) & 1
                 yield ("wait", f"wfull{j % ST}", (j // ST) & 1)
-                if WO:
+                if ACOMMIT:
                     yield ("wait", f"aempty{ab}", abph ^ 1)
                 elif j >= NB:
                     yield ("wait", f"dfull{(j - NB) % ND}", ((j - NB) // ND) & 1)
@@ -305,12 +308,14 @@ def _roles(c, st):
                         yield ("wait", f"sfull{slot}", (ch.ci // SCALE_SLOTS) & 1)
                     ready = True
                     yield ("read", f"S{slot}")
-                yield ("read", f"W{j % ST}")
                 if XC:
                     yield ("read", f"XI{j % NXR}")
                     yield ("write", f"X{ab}")
-                yield ("write", f"A{ab}")
+                # the weights go to registers first; the slot is released
+                # before they are converted into the A buffer
+                yield ("read", f"W{j % ST}")
                 yield ("arrive", f"empty{j % ST}")
+                yield ("write", f"A{ab}")
                 if XC:
                     yield ("arrive", f"xempty{j % NXR}")
                 yield ("arrive", f"afull{ab}")
@@ -353,7 +358,7 @@ def _roles(c, st):
     for grp in range(2):
         for w in range(4):
             roles.append((f"converter {grp}.{w}", converter(grp)))
-    for w in range(8):
+    for w in range(c.get("EPI", 8)):
         roles.append((f"epilogue {w}", epilogue(w)))
     return roles
 
@@ -374,10 +379,12 @@ def run(c, s0, s1, G, seed):
         sim.bar(f"aempty{i}")
     for i in range(c["ND"]):
         sim.bar(f"dfull{i}", 2 if WO else 1)
-        sim.bar(f"dempty{i}", 8)
+        sim.bar(f"dempty{i}", c.get("EPI", 8))
     for i in range(SCALE_SLOTS):
         sim.bar(f"sfull{i}")
-        sim.bar(f"sempty{i}", 8)
+        # released by the eight converter warps (weight-only) or every
+        # epilogue warp (W8A8)
+        sim.bar(f"sempty{i}", 8 if WO else c.get("EPI", 8))
     sim.bar("mma_done", 2)
     sim.bar("x_go")
     for name, gen in _roles(c, steps(s0, s1, G)):

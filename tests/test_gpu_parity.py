@@ -623,3 +623,44 @@ def test_empty_batch_is_a_no_op_everywhere():
     assert qlin.gemm_w4a16_g128_argmax(x, qw4, sb16).shape == (0,)
     torch.cuda.synchronize()
     assert qlin.device_status() == qlin.QLIN_OK
+
+
+# ------------------------------------------------ weights in the tile layout
+
+@pytest.mark.parametrize("K,N,bits", [(128, 136, 8), (5120, 1024, 8), (640, 3000, 4), (256, 8, 4)])
+def test_pack_tiles_bit_exact(K, N, bits):
+    rng = np.random.default_rng(K * N + bits)
+    qw = rng.integers(-2**31, 2**31 - 1, size=(K * bits // 32, N), dtype=np.int64).astype(np.int32)
+    t = qlin.pack_tiles(to_dev(qw), K, bits)
+    torch.cuda.synchronize()
+    assert np.array_equal(t.data.cpu().numpy(), oracle.pack_tiles(qw, K, bits))
+
+
+@pytest.mark.parametrize("M,K,N", [(8, 5120, 1024), (17, 640, 264), (64, 4096, 512), (96, 2560, 776),
+                                   (130, 512, 256), (8, 128, 40960), (1, 256, 136)])
+def test_tiled_w8a8_equals_plain_call(M, K, N):
+    """The tile layout changes only how the weight stream reads the words:
+    the outputs are those of the plain call, bit for bit, and so within the
+    tolerance of the oracle."""
+    _, qa, sa, _, qw, swb = _w8a8_inputs(31, f"gpu/tiles8/{M}/{K}/{N}", M, K, N)
+    args = (to_dev(qa), to_dev(sa))
+    sc = to_dev_bits(swb, torch.float16)
+    y_plain = qlin.gemm_w8a8_gs128(*args, to_dev(qw), sc)
+    y_tiled = qlin.gemm_w8a8_gs128_tiled(*args, qlin.pack_tiles(to_dev(qw), K, 8), sc)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev_bits(y_tiled), from_dev_bits(y_plain))
+    compare_linear(from_dev_bits(y_tiled), oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K),
+                   f"tiled w8a8 {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("M,K,N", [(8, 5120, 1024), (17, 640, 264), (64, 4096, 512), (96, 1280, 392),
+                                   (8, 128, 40960), (64, 256, 4096)])
+def test_tiled_w4a16_equals_plain_call(M, K, N):
+    xb, _, qw, sb = _w4a16_inputs(32, f"gpu/tiles4/{M}/{K}/{N}", M, K, N)
+    x, sc = to_dev_bits(xb, torch.bfloat16), to_dev_bits(sb, torch.bfloat16)
+    y_plain = qlin.gemm_w4a16_g128(x, to_dev(qw), sc)
+    y_tiled = qlin.gemm_w4a16_g128_tiled(x, qlin.pack_tiles(to_dev(qw), K, 4), sc)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev_bits(y_tiled), from_dev_bits(y_plain))
+    compare_linear(from_dev_bits(y_tiled), oracle.gemm_w4a16_g128(xb, qw, sb, K),
+                   f"tiled w4a16 {M}x{K}x{N}", "w4a16", K)

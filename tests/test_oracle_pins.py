@@ -630,3 +630,37 @@ def test_w4a16_scale_equivariance(oracle_lib):
     sb2 = bf16_of(synth.bf16_values(sb) * np.float32(2.0))
     dbl = oracle_lib.gemm_w4a16_g128(xb, qw, sb2, K)
     assert np.array_equal(dbl["y_f32"], base["y_f32"] * np.float32(2.0))
+
+
+# ------------------------------------------------------------ tile layout
+
+@pytest.mark.parametrize("K,N,bits", [(128, 128, 8), (256, 200, 8), (384, 130, 4), (128, 8, 4),
+                                      (512, 384, 8)])
+def test_pack_tiles_matches_a_reshape_of_the_words(oracle_lib, K, N, bits):
+    """The oracle's tile layout equals the GPTQ words padded to a multiple of
+    128 columns and viewed as [G, W, F, 128] with the feature-tile axis moved
+    first (an independent numpy formulation: reshape and transpose)."""
+    W = 128 * bits // 32
+    rng = np.random.default_rng(K + N + bits)
+    qw = rng.integers(-2**31, 2**31 - 1, size=(K * bits // 32, N), dtype=np.int64).astype(np.int32)
+    F = -(-N // 128)
+    padded = np.zeros((K * bits // 32, F * 128), np.int32)
+    padded[:, :N] = qw
+    want = padded.reshape(K // 128, W, F, 128).transpose(2, 0, 1, 3).reshape(-1)
+    got = oracle_lib.pack_tiles(qw, K, bits)
+    assert np.array_equal(got, want)
+
+
+def test_pack_tiles_hand_words(oracle_lib):
+    """K = 256 (two groups), N = 130 (two feature tiles, the second with two
+    live columns), 8-bit: W = 32 words per tile column.  Tile (f=1, g=1) starts
+    at word (1 * 2 + 1) * 32 * 128; its word (kk=5, j=1) is GPTQ word
+    (32 + 5, 129), and its column j = 2 is past N."""
+    K, N = 256, 130
+    qw = (np.arange(64)[:, None] * 1000 + np.arange(N)[None, :]).astype(np.int32)
+    t = oracle_lib.pack_tiles(qw, K, 8)
+    assert t.size == 2 * 2 * 32 * 128
+    base = (1 * 2 + 1) * 32 * 128
+    assert t[base + 5 * 128 + 1] == 37 * 1000 + 129
+    assert t[base + 5 * 128 + 2] == 0
+    assert t[(0 * 2 + 1) * 32 * 128 + 0 * 128 + 127] == 32 * 1000 + 127     # tile (0, 1)

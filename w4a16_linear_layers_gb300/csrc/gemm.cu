@@ -13,14 +13,14 @@
 // most 128*127*127 < 2^24, so the fp32 accumulator holds the exact integer
 // group partial.
 //
-// Structure (one persistent block of 640 threads per SM):
+// Structure (one persistent block of 640 or 768 threads per SM):
 //   * the output is cut into tiles of 128 features x T tokens; the MMA runs
 //     with the weights as operand A (128 rows = features, converted by
 //     threads straight into TMEM) and the tokens as operand B (T columns,
 //     16-bit, 128-byte swizzled in shared memory), so decode-sized M only
 //     pads T up to a multiple of 16;
 //   * W4A16 tokens (bf16) land by TMA directly in the operand layout; W8A8
-//     tokens of tiles up to 64 land as int8 tiles and the converter group of
+//     tokens of tiles up to 32 land as int8 tiles and the converter group of
 //     the step expands them exactly to fp16 beside the weights it converts
 //     (half the bytes from L2, and no extra kernel between act-quant and the
 //     GEMM); larger W8A8 tiles read an exact fp16 image written by a small
@@ -34,8 +34,8 @@
 //   * roles: warp 0 streams weights by TMA, warp 2 streams activations and
 //     group scales, warps 1 and 3 issue the MMAs of alternate steps (one
 //     thread's issue rate is below what the weight stream needs), warps 4-11
-//     convert weights into TMEM (and W8A8 tokens into fp16), warps 12-19
-//     drain TMEM.
+//     convert weights into TMEM (and W8A8 tokens into fp16), warps 12 and
+//     up drain TMEM (two per TMEM lane quarter, three at 96-token tiles).
 //
 // W8A8 per group g:  D = A_g * B_g (exact integers), then acc = fma(D, s_w, acc)
 // in the epilogue, ascending g; at the end y = bf16(acc * s_a).
@@ -57,6 +57,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "qlin_device.cuh"
@@ -65,7 +66,6 @@
 namespace qlin {
 namespace {
 
-constexpr int kThreads = 640;
 constexpr int kTileF = 128;            // features per tile = MMA M
 constexpr uint32_t kSmemLimit = 232448; // 227 KB opt-in shared memory per block
 constexpr uint32_t kCtrlBytes = 1024;
@@ -102,35 +102,40 @@ struct Cfg {
   // warps 4..11: converters, two groups of four taking alternate steps (each
   //              converts a whole 128-wide K group; warp w serves TMEM lanes
   //              32*(w%4)..)
-  // warps 12..19: epilogue, two groups of four (each drains half of the T
-  //              token columns of the accumulator)
+  // warps 12..: epilogue, kEpiPerQ warps per TMEM lane quarter, each
+  //              draining T / kEpiPerQ token columns of the accumulator, all
+  //              of them with one batch of TMEM loads (at most 32 columns, so
+  //              the loaded values and the running sums fit in registers)
   static constexpr int kConvWarp0 = 4;
   static constexpr int kConvWarps = 8;
   static constexpr int kEpiWarp0 = 12;
-  static constexpr int kEpiWarps = 8;
+  static constexpr int kEpiPerQ = T > 64 ? 3 : 2;
+  static constexpr int kEpiWarps = 4 * kEpiPerQ;
   static constexpr int kConvThreads = 32 * kConvWarps;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
+  static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
   static constexpr int kWordRows = (kInt4 ? 16 : 32) * GPS;  // int32 rows per step
   static constexpr uint32_t kWBytes = kWordRows * kTileF * 4;
   static constexpr uint32_t kABytes = 2u * T * 128u * GPS;   // 64-wide 16-bit halves
   static constexpr int kACols = 64 * GPS;                     // TMEM columns per A buffer
   // Weights and activations travel in rings of their own, so neither stream
   // waits for the other's consumer.  A weight slot is freed as soon as the
-  // converters have moved it into TMEM.
+  // converters have read it into registers.
   //   W4A16: bf16 activation tiles land by TMA in the MMA's operand layout; a
   //   slot is freed when the MMAs that read it have completed.
-  //   W8A8, T <= 64: int8 activation tiles land by TMA in a staging ring
+  //   W8A8, T <= 32: int8 activation tiles land by TMA in a staging ring
   //   (freed by the converters) and the converter group of the step expands
   //   them exactly to fp16 in the operand slot that pairs with its A buffer.
-  //   W8A8, T >= 96: that expansion would add ~36 KB of shared-memory traffic
-  //   per step on top of the MMA's own operand reads; a pre-pass kernel
-  //   writes the exact fp16 image once and its tiles land like W4A16's.
+  //   W8A8, T >= 64: that expansion would add 24-36 KB of shared-memory
+  //   traffic and a quarter of the converters' instructions per step; a
+  //   pre-pass kernel writes the exact fp16 image once and its tiles land
+  //   like W4A16's.
   // The first ring in each case is deep enough to cover the L2 latency seen
   // while the weight stream keeps HBM busy.
   static constexpr uint32_t kStageBytes = kWBytes;
   static constexpr uint32_t kXiBytes = static_cast<uint32_t>(T) * 128u;   // int8 tile
   static constexpr int kXiRaw = static_cast<int>(32768u / kXiBytes);
-  static constexpr bool kXConv = !kWO && T <= 64;
+  static constexpr bool kXConv = !kWO && T <= 32;
   static constexpr int kXiSlots = !kXConv ? 0 : (kXiRaw < 4 ? 4 : (kXiRaw > kMaxXSlots ? kMaxXSlots : kXiRaw));
   static constexpr int kXSlotsRaw = static_cast<int>(65536u / kABytes);
   static constexpr int kXSlotsW4 = kXSlotsRaw < 4 ? 4 : (kXSlotsRaw > kMaxXSlots ? kMaxXSlots : kXSlotsRaw);
@@ -144,25 +149,33 @@ struct Cfg {
   // W8A8 sizes the A buffers (converter -> MMA) and the D buffers (MMA ->
   // epilogue) separately: the epilogue loop (MMA completion, TMEM drain,
   // release) is the long one, so small token tiles get many D buffers.
-  static constexpr int kNumBufRaw = kWO ? (512 - kW4DCols) / kACols : (T <= 64 ? 4 : 2);
+  // 96-token W8A8 tiles keep four A buffers too (two per converter group, so
+  // a group converts its next step while the MMAs read its previous one),
+  // at the price of two D buffers.
+  static constexpr int kNumBufRaw = kWO ? (512 - kW4DCols) / kACols : 4;
   // An even count keeps every A buffer with one converter group and one
   // issuer (steps alternate between the two of each).
   static constexpr int kNumBufCap = kNumBufRaw < 6 ? kNumBufRaw : 6;
   static constexpr int kNumBuf = kNumBufCap - (kNumBufCap & 1);
   static constexpr int kNumDFit = kWO ? 1 : (512 - 64 * kNumBuf) / T;
   static constexpr int kNumDRaw = kNumDFit < 16 ? kNumDFit : 16;
-  // ND - NA even: see the waits of the converters
-  static constexpr int kNumD = kWO ? 1 : kNumDRaw - ((kNumDRaw - kNumBuf) & 1);
-  // W8A8 commits once per step, on the step's D buffer: that completion also
-  // frees the step's A buffer and fp16 operand slot (slot i pairs with A
-  // buffer i), which the converters wait for before they refill both.
+  // W8A8 with at least as many D buffers as A buffers commits once per step,
+  // on the step's D buffer: that completion also frees the step's A buffer
+  // and fp16 operand slot (slot i pairs with A buffer i), which the
+  // converters wait for before they refill both (ND - NA even: see the
+  // waits of the converters).  With fewer D buffers than A buffers (96-token
+  // tiles) the A buffers are freed by commits of their own, as in the
+  // weight-only formats.
+  static constexpr int kNumDEven = kNumDRaw - ((kNumDRaw - kNumBuf) & 1);
+  static constexpr int kNumD = kWO ? 1 : (kNumDRaw >= kNumBuf ? kNumDEven : kNumDRaw);
+  static constexpr bool kACommit = kWO || kNumD < kNumBuf;
   static constexpr int kXSlots = kXConv ? kNumBuf : kXSlotsW4;
-  static_assert(kWO || (kNumD >= kNumBuf && (kNumD - kNumBuf) % 2 == 0),
+  static_assert(kACommit || (kNumD >= kNumBuf && (kNumD - kNumBuf) % 2 == 0),
                 "one commit per step needs ND >= NA with ND - NA even");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColA = 0;
   static constexpr uint32_t kColD = kACols * kNumBuf;
-  static constexpr int kEpiCols = T / 2;                     // columns per epilogue thread
+  static constexpr int kEpiCols = T / kEpiPerQ;              // columns per epilogue thread
   // a weight slot is released by the four warps of one converter group
   static constexpr uint32_t kEmptyCount = kConvWarps / 2;
   // Group scales travel by TMA into a ring of their own (kScaleChunk groups x
@@ -175,11 +188,11 @@ struct Cfg {
   static constexpr uint32_t kScaleSlotBytes = kScaleRowsMax * 256u;
   static constexpr uint32_t kScaleBytes = kScales ? kScaleSlots * kScaleSlotBytes : 0u;
   static_assert(T % 16 == 0 && T >= 16 && T <= 128, "token tile");
-  static_assert(kEpiCols % 8 == 0, "epilogue columns");
+  static_assert(T % kEpiPerQ == 0 && kEpiCols % 8 == 0 && kEpiCols <= 32, "epilogue columns");
   static_assert(kNumBuf >= 2, "double buffering at least");
   static_assert(kColD + (kWO ? kW4DCols : kNumD * T) <= kTmemCols, "TMEM budget");
   static_assert(kWO || kNumD >= 2, "double buffering at least");
-  static_assert(kConvThreads == 256 && kEpiThreads == 256, "warp roles");
+  static_assert(kConvThreads == 256 && kThreads <= 1024, "warp roles");
 };
 
 constexpr int kBufMax = 6;     // A buffers
@@ -187,6 +200,13 @@ constexpr int kDBufMax = 16;   // D buffers
 
 struct KParams {
   unsigned long long* amax_keys;   // greedy-argmax variant, else nullptr
+  // Weights in the tile layout (qlin_pack_tiles): tile (f, g) of 128 features
+  // x one 128-wide K group is a contiguous block of WORDS x 128 int32
+  // (WORDS = 32 for 8-bit, 16 for 4-bit), tiles ordered by f then g, each
+  // brought in by one bulk copy.  nullptr: the GPTQ [K*bits/32, N] words by
+  // 2D tensor-map tiles.
+  const uint8_t* wtiles;
+  int64_t groups;                  // K / 128 (tile columns per feature tile)
   int s_rps;                       // W8A16: scale rows per 128-wide group (4, 1; 0 = one row)
   uint32_t s_tx;                   // bytes of one scale-chunk load
   const float* s_a;
@@ -297,6 +317,32 @@ __device__ __forceinline__ void int4x8_to_bf16x8(uint32_t w, uint32_t s2, uint32
   }
 }
 
+// N consecutive TMEM columns (N a multiple of 8) of this warp's 32 lanes into
+// v, issued as one batch; the caller waits with tmem_wait_ld.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* v) {
+  static_assert(N % 8 == 0, "columns");
+#pragma unroll
+  for (int c = 0; c + 16 <= N; c += 16) tmem_ld16(taddr + c, v + c);
+  if constexpr (N % 16 == 8) tmem_ld8(taddr + (N - 8), v + (N - 8));
+}
+
+// One step's weights into a ring slot: kWordRows x 128 int32, either one
+// contiguous bulk copy from the tile layout (the step's GPS groups are
+// consecutive tiles) or a 2D tensor-map tile of the GPTQ words.
+template <class C>
+__device__ __forceinline__ void load_weights(uint32_t dst, const CUtensorMap* tm_w, const KParams& p,
+                                             const StepIter& it, uint32_t full, uint64_t pol) {
+  if (p.wtiles != nullptr) {
+    const int64_t tile = it.f * p.groups + it.g * C::kGPS;
+    bulk_load_hint(dst, p.wtiles + tile * static_cast<int64_t>(C::kWBytes / C::kGPS), C::kWBytes, full,
+                   pol);
+  } else {
+    tma_load_2d(dst, tm_w, full, static_cast<int32_t>(it.f * kTileF),
+                static_cast<int32_t>(it.g * C::kWordRows), pol);
+  }
+}
+
 // All lanes of the warp agree on a wait's outcome.
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xFFFFFFFFu, ok); }
 
@@ -313,13 +359,13 @@ struct PendingSplit {
   int old = 0;       // arrivals before this block's (thread 0 only)
 };
 
-template <int kCols>
+template <int kCols, int kT>
 __device__ __forceinline__ void split_publish(const KParams& p, int64_t tile, int64_t cta,
                                               int64_t nC, int64_t first_tile, int colbase, int r,
                                               int et, int epi_threads, const float* vals,
                                               PendingSplit& pend) {
   const int slot = (tile == first_tile) ? 0 : 1;
-  float* mine = p.part + ((cta * 2 + slot) * (2 * kCols)) * kTileF;
+  float* mine = p.part + ((cta * 2 + slot) * kT) * kTileF;
 #pragma unroll
   for (int c = 0; c < kCols; ++c) mine[(colbase + c) * kTileF + r] = vals[c];
   named_bar_sync(1, epi_threads);
@@ -332,7 +378,7 @@ __device__ __forceinline__ void split_publish(const KParams& p, int64_t tile, in
 // (T x 128 fp32, contiguous) comes into shared memory with one bulk copy, as
 // many at a time as the idle weight and activation rings hold, so the sum
 // costs one L2 round trip per batch instead of one per column chunk.
-template <int kCols>
+template <int kCols, int kT>
 __device__ __forceinline__ bool split_finish(const KParams& p, Ctrl* ctrl, const PendingSplit& pend,
                                              int64_t nC, int colbase, int r, int et,
                                              int epi_threads, float* vals, uint32_t stage_addr,
@@ -347,7 +393,7 @@ __device__ __forceinline__ bool split_finish(const KParams& p, Ctrl* ctrl, const
   const bool last = ctrl->last_flag != 0;
   named_bar_sync(1, epi_threads);     // last_flag may be rewritten by the next call
   if (!last) return false;
-  constexpr uint32_t kPartBytes = 2u * kCols * kTileF * sizeof(float);
+  constexpr uint32_t kPartBytes = static_cast<uint32_t>(kT) * kTileF * sizeof(float);
   const int64_t cap = static_cast<int64_t>(stage_bytes / kPartBytes);
 #pragma unroll
   for (int c = 0; c < kCols; ++c) vals[c] = 0.0f;
@@ -367,7 +413,7 @@ __device__ __forceinline__ bool split_finish(const KParams& p, Ctrl* ctrl, const
         const int64_t cc = b0 + i;
         const int slot = ((cc * p.W / nC) / G == tile) ? 0 : 1;
         bulk_load(stage_addr + static_cast<uint32_t>(i) * kPartBytes,
-                  p.part + ((cc * 2 + slot) * (2 * kCols)) * kTileF, kPartBytes, full);
+                  p.part + ((cc * 2 + slot) * kT) * kTileF, kPartBytes, full);
       }
     }
     ok = warp_all(mbar_wait(smem_u32(&ctrl->fix_full), fix_phase, ctx, 18));
@@ -387,7 +433,7 @@ __device__ __forceinline__ bool split_finish(const KParams& p, Ctrl* ctrl, const
 }
 
 template <int kMode, int T, int GPS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
     qlin_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                      const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_s, const KParams p) {
@@ -442,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < SR; ++i) {
       mbar_init(smem_u32(&ctrl->s_full[i]), 1);
-      mbar_init(smem_u32(&ctrl->s_empty[i]), 8);
+      // released by every converter warp (weight-only) or epilogue warp (W8A8)
+      mbar_init(smem_u32(&ctrl->s_empty[i]), C::kWO ? C::kConvWarps : C::kEpiWarps);
     }
     mbar_init(smem_u32(&ctrl->mma_done), C::kIssuers);
     mbar_init(smem_u32(&ctrl->x_go), 1);
@@ -454,16 +501,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // set-up barrier (every slot is free, so no wait is needed).  Only a few:
     // every TMA load of the SM queues behind the ones issued before it, and
     // the first activation tiles must not wait behind a full weight ring.
-    prefetch_tmap(&tm_w);
+    if (p.wtiles == nullptr) prefetch_tmap(&tm_w);
     StepIter it(s0, G, F);
     const int pre = kPreW < stages ? kPreW : stages;
     const int first = n_steps < pre ? n_steps : pre;
     for (int j = 0; j < first; ++j, it.next()) {
       const uint32_t full = smem_u32(&ctrl->wfull[j]);
       mbar_arrive_expect_tx(full, C::kWBytes);
-      tma_load_2d(sbase + static_cast<uint32_t>(j) * C::kStageBytes, &tm_w, full,
-                  static_cast<int32_t>(it.f * kTileF), static_cast<int32_t>(it.g * C::kWordRows),
-                  pol_w);
+      load_weights<C>(sbase + static_cast<uint32_t>(j) * C::kStageBytes, &tm_w, p, it, full, pol_w);
     }
     w_issued = first;
   }
@@ -500,9 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(smem_u32(&ctrl->empty[rg.slot]), rg.phase ^ 1u, ctx, 1)) break;
         const uint32_t full = smem_u32(&ctrl->wfull[rg.slot]);
         mbar_arrive_expect_tx(full, C::kWBytes);
-        tma_load_2d(sbase + static_cast<uint32_t>(rg.slot) * C::kStageBytes, &tm_w, full,
-                    static_cast<int32_t>(it.f * kTileF), static_cast<int32_t>(it.g * C::kWordRows),
-                    pol_w);
+        load_weights<C>(sbase + static_cast<uint32_t>(rg.slot) * C::kStageBytes, &tm_w, p, it, full,
+                        pol_w);
         ++w_issued;
       }
       // Every load issued must land before the block exits.
@@ -622,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(dcol, tmem + C::kColA + ab * C::kACols + ks * 8, d0 + (off >> 4), idesc,
                    acc ? 1u : 0u);
           }
-          if constexpr (C::kWO) tc_commit(smem_u32(&ctrl->a_empty[ab]));
+          if constexpr (C::kACommit) tc_commit(smem_u32(&ctrl->a_empty[ab]));
           if constexpr (!C::kXConv) tc_commit(smem_u32(&ctrl->xempty[rx.slot]));
           // W8A8: also frees the A buffer (and the fp16 slot of in-kernel expansion)
           if constexpr (!C::kWO) tc_commit(smem_u32(&ctrl->d_full[db]));
@@ -671,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ab = j % NB;
         const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
         bool ok = mbar_wait(smem_u32(&ctrl->wfull[rg.slot]), rg.phase, ctx, 7);
-        if constexpr (C::kWO) {
+        if constexpr (C::kACommit) {
           if (ok) ok = mbar_wait(smem_u32(&ctrl->a_empty[ab]), abph ^ 1u, ctx, 8);
         } else if (ok && j >= NB) {
           // A buffer ab was last read by step j - NB, committed on its D
@@ -737,19 +781,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* wsm = reinterpret_cast<const uint32_t*>(
             smem + static_cast<uint32_t>(rg.slot) * C::kStageBytes);
         const uint32_t acol = tmem + lane_off + C::kColA + ab * C::kACols;
+        // Every word this thread converts in the step, loaded before the
+        // first TMEM store (the stores' ordering would otherwise hold each
+        // batch of shared-memory loads back behind the previous batch's
+        // conversion); the weight slot is then free for the next load.
+        uint32_t wreg[C::kWordRows];
+#pragma unroll
+        for (int i = 0; i < C::kWordRows; ++i) wreg[i] = wsm[i * kTileF + r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl->empty[rg.slot]));
 #pragma unroll
         for (int h = 0; h < 4 * GPS; ++h) {
           uint32_t v[16];
           if constexpr (C::kInt4) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              int4x8_to_bf16x8(wsm[(h * 4 + i) * kTileF + r], s2g[h >> 2], v + 4 * i);
+            for (int i = 0; i < 4; ++i) int4x8_to_bf16x8(wreg[h * 4 + i], s2g[h >> 2], v + 4 * i);
           } else if constexpr (kMode == kModeW8A16) {
             // byte u = q + 128 -> exact q in fp32 (2^23 + u minus 2^23 + 128),
             // q * s exact in fp32, one rounding to bf16
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const uint32_t w = wsm[(h * 8 + i) * kTileF + r];
+              const uint32_t w = wreg[h * 8 + i];
               float f[4];
 #pragma unroll
               for (int b = 0; b < 4; ++b)
@@ -760,8 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              biased_u8x4_to_f16x4(wsm[(h * 8 + i) * kTileF + r], v[2 * i], v[2 * i + 1]);
+            for (int i = 0; i < 8; ++i) biased_u8x4_to_f16x4(wreg[h * 8 + i], v[2 * i], v[2 * i + 1]);
           }
           tmem_st16(acol + h * 16, v);
         }
@@ -769,7 +820,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(smem_u32(&ctrl->empty[rg.slot]));
           if constexpr (C::kXConv) mbar_arrive(smem_u32(&ctrl->xempty[ri.slot]));
           mbar_arrive(smem_u32(&ctrl->a_full[ab]));
         }
@@ -798,7 +848,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;                  // TMEM lane = feature in tile
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int colbase = ((warp - C::kEpiWarp0) >> 2) * C::kEpiCols;
-    constexpr int kCh = C::kEpiCols < 16 ? C::kEpiCols : 16;
     const int64_t M = p.M, N = p.N;
     const int64_t first_tile = s0 / G;
     uint16_t* y = static_cast<uint16_t*>(p.out);
@@ -895,45 +944,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t dcol = tmem + lane_off + C::kColD + colbase +
                                 (C::kWO ? b * C::kIssuers * T : b * T);
+          constexpr int E = C::kEpiCols;
+          uint32_t v[E];
+          if constexpr (C::kWO) {
+            // the issuers' accumulators, summed in issuer order; an issuer
+            // that took no step of this segment left its accumulator unused
+            const bool both = j > seg_j0;
+            const int only = seg_j0 & 1;
+            if (both) {
+              tmem_ld_cols<E>(dcol, v);
+              tmem_ld_cols<E>(dcol + T, reinterpret_cast<uint32_t*>(acc));
+              tmem_wait_ld();
 #pragma unroll
-          for (int c0 = 0; c0 < C::kEpiCols; c0 += kCh) {
-            uint32_t v[kCh];
-            if constexpr (kCh == 16) tmem_ld16(dcol + c0, v);
-            else tmem_ld8(dcol + c0, v);
+              for (int c = 0; c < E; ++c) acc[c] = __uint_as_float(v[c]) + acc[c];
+            } else {
+              tmem_ld_cols<E>(dcol + (only == 0 ? 0u : static_cast<uint32_t>(T)),
+                              reinterpret_cast<uint32_t*>(acc));
+              tmem_wait_ld();
+            }
+          } else {
+            // all of this thread's columns in one batch of loads, one wait
+            tmem_ld_cols<E>(dcol, v);
             tmem_wait_ld();
-            if constexpr (C::kWO) {
-              // the issuers' accumulators, summed in issuer order; an issuer
-              // that took no step of this segment left its accumulator unused
-              const bool both = j > seg_j0;
-              const int only = seg_j0 & 1;
-              if (both || only == 0) {
-#pragma unroll
-                for (int c = 0; c < kCh; ++c) acc[c0 + c] = __uint_as_float(v[c]);
-              }
-              if (both || only == 1) {
-                uint32_t v1[kCh];
-                if constexpr (kCh == 16) tmem_ld16(dcol + T + c0, v1);
-                else tmem_ld8(dcol + T + c0, v1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < kCh; ++c)
-                  acc[c0 + c] = both ? acc[c0 + c] + __uint_as_float(v1[c]) : __uint_as_float(v1[c]);
-              }
-            } else if constexpr (kMode == kModeP) {
+            if constexpr (kMode == kModeP) {
               if (!waited) {
                 grid_dep_wait();
                 waited = true;
               }
               int32_t* P = static_cast<int32_t*>(p.out);
 #pragma unroll
-              for (int c = 0; c < kCh; ++c) {
-                const int64_t m = t * T + colbase + c0 + c;
+              for (int c = 0; c < E; ++c) {
+                const int64_t m = t * T + colbase + c;
                 if (m < M && n < N)
                   P[(g * M + m) * N + n] = static_cast<int32_t>(__uint_as_float(v[c]));
               }
             } else {
 #pragma unroll
-              for (int c = 0; c < kCh; ++c) acc[c0 + c] = fmaf(__uint_as_float(v[c]), sw, acc[c0 + c]);
+              for (int c = 0; c < E; ++c) acc[c] = fmaf(__uint_as_float(v[c]), sw, acc[c]);
             }
           }
           tc_fence_before();
@@ -955,7 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (full_tile) {
         write_out(t, n, acc);
       } else {
-        split_publish<C::kEpiCols>(p, tile, cta, nC, first_tile, colbase, r, et, C::kEpiThreads,
+        split_publish<C::kEpiCols, T>(p, tile, cta, nC, first_tile, colbase, r, et, C::kEpiThreads,
                                    acc, pend[npend]);
         ++npend;
       }
@@ -965,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (named_bar_and(2, C::kEpiThreads, alive)) {
       uint32_t fix_phase = 0;
       for (int k = 0; k < npend; ++k) {
-        if (split_finish<C::kEpiCols>(p, ctrl, pend[k], nC, colbase, r, et, C::kEpiThreads, acc,
+        if (split_finish<C::kEpiCols, T>(p, ctrl, pend[k], nC, colbase, r, et, C::kEpiThreads, acc,
                                       sbase, reinterpret_cast<const float*>(smem), sc_off,
                                       fix_phase, drain_ctx)) {
           const int64_t tt = pend[k].tile / F;
@@ -1005,7 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // int8 activations -> fp16 (exact), 16 values per thread: the B operand of
-// the W8A8 GEMM at token tiles of 96 and more.  Waits for its predecessor
+// the W8A8 GEMM at token tiles of 64 and more.  Waits for its predecessor
 // before touching memory (the previous GEMM may still read this buffer), then
 // lets the GEMM start.
 __global__ void __launch_bounds__(256) act_i8_to_f16_kernel(const int8_t* __restrict__ q,
@@ -1117,10 +1164,13 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl_in, int* err, cudaStr
   }
   CUtensorMap tw, ta;
   const uint64_t words_rows = static_cast<uint64_t>(a.K) / (C::kInt4 ? 8 : 4);
-  if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, a.qweight, a.N, words_rows,
-                   static_cast<uint64_t>(a.N) * 4, kTileF, C::kWordRows,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+  if (a.wtiles != nullptr) {
+    std::memset(&tw, 0, sizeof(tw));   // not read: the tiles come by bulk copies
+  } else if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_INT32, a.qweight, a.N, words_rows,
+                          static_cast<uint64_t>(a.N) * 4, kTileF, C::kWordRows,
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) {
     return cudaErrorInvalidValue;
+  }
   if constexpr (!C::kXConv) {
     if (!make_act_map(&ta, C::kWO ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                       act16, a.M, a.K, T, 2 * GPS))
@@ -1165,6 +1215,8 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl_in, int* err, cudaStr
 
   KParams kp;
   kp.amax_keys = a.amax_keys;
+  kp.wtiles = reinterpret_cast<const uint8_t*>(a.wtiles);
+  kp.groups = a.K / kGroup;
   kp.s_rps = s_rps;
   kp.s_tx = s_box * 256u;
   kp.s_a = a.s_a;
@@ -1180,7 +1232,7 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl_in, int* err, cudaStr
   kp.limit_ns = kWaitLimitNs;
   kp.stages = stages;
   return launch_pdl(qlin_gemm_kernel<kMode, T, GPS>, dim3(static_cast<unsigned>(pl.ctas)),
-                    dim3(kThreads), smem, stream, tw, ta, ts, kp);
+                    dim3(C::kThreads), smem, stream, tw, ta, ts, kp);
 }
 
 template <int kMode>
@@ -1233,10 +1285,10 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
   // any shape that share a workspace never see each other's partials there.
   p.counter_bytes = kCounterBytes;
   const size_t partial_bytes = static_cast<size_t>(p.ctas) * 2 * p.T * kTileF * sizeof(float);
-  // then, for token tiles of 96 and more, the fp16 image of the W8A8
+  // then, for token tiles of 64 and more, the fp16 image of the W8A8
   // activations (1 KB aligned)
   p.act_offset = (p.counter_bytes + partial_bytes + 1023) & ~static_cast<size_t>(1023);
-  p.workspace_bytes = p.T >= 96 ? p.act_offset + static_cast<size_t>(M) * static_cast<size_t>(K) * 2
+  p.workspace_bytes = p.T >= 64 ? p.act_offset + static_cast<size_t>(M) * static_cast<size_t>(K) * 2
                                 : p.counter_bytes + partial_bytes;
   return p;
 }

@@ -57,6 +57,28 @@ __global__ void wait_timeout_kernel(int64_t limit_ns, int* err) {
   }
 }
 
+// The tile layout of the GEMMs' weight stream: tile (f, g) holds the words
+// of feature tile f (128 output features) and K group g (128 K values) as a
+// contiguous block of W x 128 int32 (W = 32 words for 8-bit, 16 for 4-bit),
+// word (kk, nl) of the tile = GPTQ word (g*W + kk, f*128 + nl); tiles are
+// ordered by f, then g.  Features past N in the last tile hold 0 (never
+// output).  One thread per tile word; the reads of a warp are 32 consecutive
+// GPTQ words of one row and its writes 32 consecutive tile words.
+__global__ void tiles_kernel(const int32_t* __restrict__ qweight, int64_t N, int64_t G, int words_per_group,
+                             int64_t total, int32_t* __restrict__ tiles) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t nl = i & 127;
+    const int64_t row = i >> 7;                    // (tile, kk)
+    const int64_t tile = row / words_per_group;
+    const int64_t kk = row - tile * words_per_group;
+    const int64_t f = tile / G;
+    const int64_t g = tile - f * G;
+    const int64_t n = f * 128 + nl;
+    tiles[i] = n < N ? qweight[(g * words_per_group + kk) * N + n] : 0;
+  }
+}
+
 unsigned grid_for(int64_t n, int threads) {
   int64_t blocks = (n + threads - 1) / threads;
   if (blocks > 65535LL * 16) blocks = 65535LL * 16;
@@ -117,6 +139,19 @@ cudaError_t launch_pack(const int8_t* q, int64_t K, int64_t N, int bits, int32_t
   const int64_t zwords = (K / kGroup) * (N / per);
   const uint32_t zword = bits == 8 ? 0x80808080u : 0x88888888u;
   fill_kernel<<<grid_for(zwords, 256), 256, 0, stream>>>(qzeros, zwords, zword);
+  return cudaGetLastError();
+}
+
+size_t tiles_bytes(int64_t K, int64_t N, int bits) {
+  const int64_t F = (N + 127) / 128;
+  return static_cast<size_t>(F) * static_cast<size_t>(K) * 128u * static_cast<size_t>(bits) / 8u;
+}
+
+cudaError_t launch_pack_tiles(const int32_t* qweight, int64_t K, int64_t N, int bits,
+                              int32_t* tiles, cudaStream_t stream) {
+  const int wpg = kGroup * bits / 32;
+  const int64_t total = static_cast<int64_t>(tiles_bytes(K, N, bits) / 4);
+  tiles_kernel<<<grid_for(total, 256), 256, 0, stream>>>(qweight, N, K / kGroup, wpg, total, tiles);
   return cudaGetLastError();
 }
 

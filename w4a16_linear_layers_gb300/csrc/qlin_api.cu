@@ -81,9 +81,9 @@ qlin_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLI
 qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const int32_t* qweight,
                        const uint16_t* scales, void* out, int64_t M, int64_t N, int64_t K,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                       int group_size = 128) {
+                       int group_size = 128, bool tiled = false) {
   // an empty batch reads and writes nothing: its activation, scale and
-  // output pointers may be NULL
+  // output pointers may be NULL.  `tiled`: qweight holds the tile layout.
   const bool rows = M != 0;
   if ((rows && (act == nullptr || out == nullptr || (mode == GemmMode::kW8A8 && s_a == nullptr))) ||
       qweight == nullptr || (mode != GemmMode::kW8A8Partials && scales == nullptr))
@@ -102,6 +102,7 @@ qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const i
   if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return QLIN_ERR_WORKSPACE;
   GemmArgs a{mode, act, s_a, qweight, scales, out, M, N, K, workspace, workspace_bytes};
   a.group_size = group_size;
+  if (tiled) a.wtiles = qweight;
   return from_cuda(launch_gemm(a, plan, d->err_word, stream));
 }
 
@@ -198,6 +199,22 @@ qlin_status_t qlin_gemm_w8a8_gs128(const int8_t* q_a, const float* s_a, const in
                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+qlin_status_t qlin_gemm_w8a8_gs128_tiled(const int8_t* q_a, const float* s_a, const int32_t* tiles,
+                                         const uint16_t* scales, int64_t M, int64_t N, int64_t K,
+                                         uint16_t* y, void* workspace, size_t workspace_bytes,
+                                         qlin_stream_t stream) {
+  return run_gemm(GemmMode::kW8A8, q_a, s_a, tiles, scales, y, M, N, K, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream), 128, true);
+}
+
+qlin_status_t qlin_gemm_w4a16_g128_tiled(const uint16_t* x, const int32_t* tiles,
+                                         const uint16_t* scales, int64_t M, int64_t N, int64_t K,
+                                         uint16_t* y, void* workspace, size_t workspace_bytes,
+                                         qlin_stream_t stream) {
+  return run_gemm(GemmMode::kW4A16, x, nullptr, tiles, scales, y, M, N, K, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream), 128, true);
+}
+
 qlin_status_t qlin_gemm_w4a16_g128(const uint16_t* x, const int32_t* qweight,
                                    const uint16_t* scales, int64_t M, int64_t N, int64_t K,
                                    uint16_t* y, void* workspace, size_t workspace_bytes,
@@ -271,6 +288,27 @@ qlin_status_t qlin_pack_gptq(const int8_t* q, int64_t K, int64_t N, int bits, in
                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t qlin_tiles_bytes(int64_t K, int64_t N, int bits) {
+  if ((bits != 4 && bits != 8) || N < 1 || N > kMaxDim || K < kGroup || K > kMaxDim ||
+      (K % kGroup) != 0)
+    return 0;
+  return tiles_bytes(K, N, bits);
+}
+
+qlin_status_t qlin_pack_tiles(const int32_t* qweight, int64_t K, int64_t N, int bits,
+                              int32_t* tiles, qlin_stream_t stream) {
+  if (qweight == nullptr || tiles == nullptr) return QLIN_ERR_NULL;
+  if (bits != 4 && bits != 8) return QLIN_ERR_BITS;
+  if (N < 1 || N > kMaxDim || K < kGroup || K > kMaxDim || (K % kGroup) != 0)
+    return QLIN_ERR_SHAPE;
+  if (!aligned16(qweight) || !aligned16(tiles)) return QLIN_ERR_ALIGN;
+  const DeviceInfo* d = nullptr;
+  qlin_status_t st = device_or_error(&d);
+  if (st != QLIN_OK) return st;
+  return from_cuda(launch_pack_tiles(qweight, K, N, bits, tiles,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t qlin_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (check_gemm_shape(M, N, K) != QLIN_OK || M == 0) return 0;
   const DeviceInfo* d = current_device();
@@ -338,6 +376,6 @@ const char* qlin_status_string(qlin_status_t status) {
   }
 }
 
-int qlin_version(void) { return 101; }
+int qlin_version(void) { return 102; }
 
 }  // extern "C"

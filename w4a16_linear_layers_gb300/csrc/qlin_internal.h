@@ -39,6 +39,12 @@ cudaError_t launch_ingest_nk(const int32_t* packed_nk, const uint16_t* scales_ng
                              int64_t N, int bits, int32_t* qweight, uint16_t* scales,
                              cudaStream_t stream);
 
+// Bytes of the tile layout of a [K*bits/32, N] GPTQ weight matrix, and the
+// repack into it (see tiles_kernel in pack.cu).
+size_t tiles_bytes(int64_t K, int64_t N, int bits);
+cudaError_t launch_pack_tiles(const int32_t* qweight, int64_t K, int64_t N, int bits,
+                              int32_t* tiles, cudaStream_t stream);
+
 // GEMM problem description passed from the API to the launcher.
 enum class GemmMode : int { kW8A8 = 0, kW8A8Partials = 1, kW4A16 = 2, kW8A16 = 3 };
 
@@ -58,6 +64,8 @@ struct GemmArgs {
   unsigned long long* amax_keys = nullptr;
   // W8A16: K-width of a scale group (32 or 128), or 0 for one scale per column
   int group_size = 128;
+  // Weights in the tile layout (qweight is then unused), else nullptr.
+  const int32_t* wtiles = nullptr;
 };
 
 // Offset of the argmax keys (one per row, M <= 96) inside the fixed counter
@@ -79,7 +87,7 @@ struct GemmPlan {
   int64_t steps;   // TT * F * G
   int64_t ctas;    // grid size
   size_t counter_bytes;
-  size_t act_offset;     // fp16 image of the W8A8 activations (token tiles >= 96)
+  size_t act_offset;     // fp16 image of the W8A8 activations (token tiles >= 64)
   size_t workspace_bytes;
 };
 

@@ -37,6 +37,10 @@ EXPORTS = (
     "qlin_gemm_w8a8_gs128",
     "qlin_gemm_w8a8_gs128_noalloc",
     "qlin_gemm_w4a16_g128",
+    "qlin_gemm_w8a8_gs128_tiled",
+    "qlin_gemm_w4a16_g128_tiled",
+    "qlin_tiles_bytes",
+    "qlin_pack_tiles",
     "qlin_gemm_w8a16",
     "qlin_gemm_w8a8_gs128_argmax",
     "qlin_gemm_w4a16_g128_argmax",
@@ -86,6 +90,10 @@ def load():
             "qlin_gemm_w8a8_gs128_noalloc": ([P, P, P, P, I64, I64, I64, P, P], I),
             "qlin_gemm_w4a16_g128": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_gemm_w8a16": ([P, P, P, I64, I64, I64, I, P, P, SZ, P], I),
+            "qlin_gemm_w8a8_gs128_tiled": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_gemm_w4a16_g128_tiled": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_tiles_bytes": ([I64, I64, I], SZ),
+            "qlin_pack_tiles": ([P, I64, I64, I, P, P], I),
             "qlin_gemm_w8a8_gs128_argmax": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_gemm_w4a16_g128_argmax": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_pack_gptq": ([P, I64, I64, I, P, P, P], I),
@@ -304,6 +312,72 @@ def gemm_w4a16_g128(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor
     ws = _workspace(workspace, M, N, K, x.device)
     _check(load().qlin_gemm_w4a16_g128(_ptr(x), _ptr(qweight), _ptr(scales), M, N, K, _ptr(y),
                                        _ptr(ws), ws.numel(), _stream_handle(stream)))
+    return y
+
+
+class Tiles:
+    """Weights in the tile layout of qlin_pack_tiles: the flat int32 device
+    tensor and the shape of the matrix it holds (K, N, bits)."""
+
+    def __init__(self, data: torch.Tensor, K: int, N: int, bits: int):
+        self.data, self.K, self.N, self.bits = data, int(K), int(N), int(bits)
+
+
+def tiles_bytes(K: int, N: int, bits: int) -> int:
+    return int(load().qlin_tiles_bytes(int(K), int(N), int(bits)))
+
+
+def pack_tiles(qweight: torch.Tensor, K: int, bits: int, stream=None) -> Tiles:
+    """GPTQ words [K*bits/32, N] -> the tile layout (one contiguous block per
+    128-feature x 128-K tile)."""
+    _need(qweight, "qweight", torch.int32, 2)
+    N = qweight.shape[1]
+    if qweight.shape[0] * (32 // bits) != K:
+        raise ValueError("qweight rows do not match K and bits")
+    nbytes = tiles_bytes(K, N, bits)
+    if nbytes == 0:
+        raise ValueError("invalid shape or bits for the tile layout")
+    data = torch.empty(nbytes // 4, dtype=torch.int32, device=qweight.device)
+    _check(load().qlin_pack_tiles(_ptr(qweight), K, N, bits, _ptr(data), _stream_handle(stream)))
+    return Tiles(data, K, N, bits)
+
+
+def gemm_w8a8_gs128_tiled(q_a: torch.Tensor, s_a: torch.Tensor, tiles: Tiles,
+                          scales: torch.Tensor, y: torch.Tensor | None = None, workspace=None,
+                          stream=None) -> torch.Tensor:
+    """gemm_w8a8_gs128 with the weights in the tile layout (pack_tiles, bits 8)."""
+    _need(q_a, "q_a", torch.int8, 2)
+    _need(s_a, "s_a", torch.float32, 1)
+    _need(scales, "scales", torch.float16, 2)
+    M, K = q_a.shape
+    N = tiles.N
+    if tiles.bits != 8 or tiles.K != K or scales.shape != (K // 128, N) or s_a.shape[0] != M:
+        raise ValueError("inconsistent W8A8 shapes")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=q_a.device)
+    _need(y, "y", torch.bfloat16, 2)
+    ws = _workspace(workspace, M, N, K, q_a.device)
+    _check(load().qlin_gemm_w8a8_gs128_tiled(_ptr(q_a), _ptr(s_a), _ptr(tiles.data), _ptr(scales),
+                                             M, N, K, _ptr(y), _ptr(ws), ws.numel(),
+                                             _stream_handle(stream)))
+    return y
+
+
+def gemm_w4a16_g128_tiled(x: torch.Tensor, tiles: Tiles, scales: torch.Tensor,
+                          y: torch.Tensor | None = None, workspace=None, stream=None) -> torch.Tensor:
+    """gemm_w4a16_g128 with the weights in the tile layout (pack_tiles, bits 4)."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(scales, "scales", torch.bfloat16, 2)
+    M, K = x.shape
+    N = tiles.N
+    if tiles.bits != 4 or tiles.K != K or scales.shape != (K // 128, N):
+        raise ValueError("inconsistent W4A16 shapes")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", torch.bfloat16, 2)
+    ws = _workspace(workspace, M, N, K, x.device)
+    _check(load().qlin_gemm_w4a16_g128_tiled(_ptr(x), _ptr(tiles.data), _ptr(scales), M, N, K,
+                                             _ptr(y), _ptr(ws), ws.numel(), _stream_handle(stream)))
     return y
 
 
