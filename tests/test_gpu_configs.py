@@ -119,6 +119,33 @@ def test_vocab_head_w8a8(M):
     run_w8a8("lm_head", M, 5120, 248320, "outliers", argmax=True)
 
 
+@pytest.mark.parametrize("M", [8, 96])
+def test_vocab_head_w4a16_argmax(M):
+    """The INT4 g128 vocabulary head of the DFlash2 decoding recipe at full
+    size (5120 -> 248320), plain and with the fused greedy argmax.  The 1.27 G
+    weights are drawn on the device from the generator's stream (bit for bit
+    the host's) and packed there; the oracle takes the sampled columns'
+    weights from the host generator and packs them itself."""
+    name, K, N, seed = "lm_head", 5120, 248320, 0
+    xb = synth.activations(seed, f"{name}/w4/M{M}", M, K, "normal")
+    q_d = synth.randint_device(seed, name + "/w4/qw", (K, N), -7, 7, "cuda")
+    qw_d, _ = qlin.pack_gptq(q_d, 4, with_qzeros=False)
+    del q_d
+    sb = synth.bf16_bits(synth.log_uniform(seed, name + "/w4/sw", (K // 128, N), 1e-3, 3e-2))
+    x_d, sb_d = to_dev_bits(xb, torch.bfloat16), to_dev_bits(sb, torch.bfloat16)
+    y_d = qlin.gemm_w4a16_g128(x_d, qw_d, sb_d)
+    idx = qlin.gemm_w4a16_g128_argmax(x_d, qw_d, sb_d)
+    want = y_d.float().argmax(dim=1).to(torch.int32)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, want), f"M={M}: fused W4A16 argmax differs from the plain call's"
+    rows, cols = sample_rows(M, seed), sample_cols(N, seed)
+    q_cols = synth.randint_at(seed, name + "/w4/qw", N, np.arange(K), cols, -7, 7)
+    qw_cols, _, _ = oracle.pack_gptq(np.ascontiguousarray(q_cols), 4)
+    ref = oracle.gemm_w4a16_g128(xb, qw_cols, np.ascontiguousarray(sb[:, cols]), K, rows)
+    y = from_dev_bits(y_d)[np.ix_(rows, cols)]
+    compare_linear(y, ref, f"lm_head w4a16 M={M}", "w4a16", K)
+
+
 @pytest.mark.parametrize("M", [8, 64, 96])
 def test_fused_gate_up_full_size_w8a8(M):
     """gate_proj and up_proj as one GEMM over their weights concatenated along

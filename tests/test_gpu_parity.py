@@ -664,3 +664,28 @@ def test_tiled_w4a16_equals_plain_call(M, K, N):
     assert np.array_equal(from_dev_bits(y_tiled), from_dev_bits(y_plain))
     compare_linear(from_dev_bits(y_tiled), oracle.gemm_w4a16_g128(xb, qw, sb, K),
                    f"tiled w4a16 {M}x{K}x{N}", "w4a16", K)
+
+
+# ------------------------------------------- many token tiles: banded whole tiles
+
+@pytest.mark.parametrize("M,K,N", [(600, 384, 776), (1000, 256, 264), (1500, 17408, 136)])
+def test_banded_tile_schedule_w8a8(M, K, N):
+    """Batches of six or more token tiles take whole tiles in bands of token
+    tiles (one band at K = 384 and 256; at K = 17408 the bands hold 14 token
+    tiles, so the 16 token tiles make a full band and a ragged one).  No tile
+    is split, every output is written once, and the fp32 chain is the
+    oracle's."""
+    _, qa, sa, _, qw, swb = _w8a8_inputs(33, f"gpu/band8/{M}/{K}/{N}", M, K, N)
+    y = _gemm_w8a8_gpu(qa, sa, qw, swb)
+    rows = np.concatenate([np.arange(0, M, 7), [M - 1]])
+    ref = oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K, rows)
+    compare_linear(np.ascontiguousarray(y[rows]), ref, f"banded w8a8 {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("M,K,N", [(600, 384, 776), (1500, 17408, 136)])
+def test_banded_tile_schedule_w4a16(M, K, N):
+    xb, _, qw, sb = _w4a16_inputs(34, f"gpu/band4/{M}/{K}/{N}", M, K, N)
+    y = _gemm_w4a16_gpu(xb, qw, sb)
+    rows = np.concatenate([np.arange(0, M, 7), [M - 1]])
+    ref = oracle.gemm_w4a16_g128(xb, qw, sb, K, rows)
+    compare_linear(np.ascontiguousarray(y[rows]), ref, f"banded w4a16 {M}x{K}x{N}", "w4a16", K)

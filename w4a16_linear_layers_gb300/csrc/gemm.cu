@@ -77,6 +77,8 @@ constexpr uint32_t kArgBytes = 4096;     // shared argmax keys: [4 lane quarters
 constexpr int64_t kMinSteps = 8;          // minimum (tile, group) steps per block
 constexpr int kScaleChunk = 8;            // groups of scales per TMA load
 constexpr int kPreW = 3;                  // weight loads issued before the first activations
+constexpr int64_t kBandMinTiles = 6;      // token tiles from which whole tiles go in bands
+constexpr int64_t kBandBytes = 48ll << 20;   // activation bytes of one band
 
 constexpr int kModeW8A8 = 0;
 constexpr int kModeP = 1;     // W8A8 pipeline, exports the group partials
@@ -212,6 +214,8 @@ struct KParams {
   const float* s_a;
   void* out;
   int64_t M, N, G, F, W;
+  int64_t TT;                      // token tiles
+  int64_t band;                    // banded-tile schedule: token tiles per band; 0 = stream-K
   float* part;
   int* counters;
   int* err;
@@ -247,21 +251,47 @@ __device__ __forceinline__ int64_t cta_of_step(int64_t s, int64_t C, int64_t W) 
   return ((s + 1) * C + W - 1) / W - 1;
 }
 
-// Walks a block's (tile, group) steps without dividing: g is the group, f the
-// feature tile and t the token tile of the current step.
+// Walks a block's (tile, group) steps: g is the group, f the feature tile
+// and t the token tile of the current step.  Two schedules:
+//  * stream-K (band == 0): the block's contiguous range of the step list,
+//    tiles in token-tile-major order, a range may start and end mid-tile;
+//  * banded tiles (band > 0, batches of many token tiles): block c takes whole
+//    tiles c, c + C, c + 2C, ... of an order that walks bands of `band` token
+//    tiles: within a band, feature tile by feature tile, every token tile of
+//    the band.  The blocks running at one time then share a few feature
+//    tiles' weights and one band's activations, which L2 holds, instead of
+//    each block streaming every weight tile once per token tile from DRAM.
 struct StepIter {
-  int64_t G, F, g, f, t;
-  __device__ __forceinline__ StepIter(int64_t s0, int64_t G_, int64_t F_) : G(G_), F(F_) {
-    const int64_t tile = s0 / G;
-    g = s0 - tile * G;
-    t = tile / F;
-    f = tile - t * F;
+  int64_t G, F, TT, band, C;
+  int64_t g, f, t, q;   // q: the tile's index in the schedule's order
+  __device__ __forceinline__ StepIter(const KParams& p, int64_t s0)
+      : G(p.G), F(p.F), TT(p.TT), band(p.band), C(gridDim.x) {
+    if (band > 0) {
+      g = 0;
+      q = blockIdx.x;
+      place();
+    } else {
+      q = s0 / G;
+      g = s0 - q * G;
+      t = q / F;
+      f = q - t * F;
+    }
   }
-  __device__ __forceinline__ int64_t tile() const { return t * F + f; }
+  __device__ __forceinline__ void place() {   // banded order: q -> (f, t)
+    const int64_t b = q / (band * F);
+    const int64_t r = q - b * band * F;
+    const int64_t rows = (TT - b * band) < band ? (TT - b * band) : band;
+    f = r / rows;
+    t = b * band + (r - f * rows);
+  }
+  __device__ __forceinline__ int64_t tile() const { return band > 0 ? q : t * F + f; }
   __device__ __forceinline__ void next() {
     if (++g == G) {
       g = 0;
-      if (++f == F) {
+      if (band > 0) {
+        q += C;
+        if (q < TT * F) place();
+      } else if (++f == F) {
         f = 0;
         ++t;
       }
@@ -460,12 +490,18 @@ __global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int64_t nC = gridDim.x;
   const int64_t cta = blockIdx.x;
-  const int64_t s0 = cta * p.W / nC;
-  const int64_t s1 = (cta + 1) * p.W / nC;
-  const int n_steps = static_cast<int>(s1 - s0);
+  // stream-K: the block's range [s0, s1) of the step list; banded tiles: the
+  // block's whole tiles cta, cta + nC, ... (s0 unused)
+  const int64_t s0 = p.band > 0 ? 0 : cta * p.W / nC;
+  const int64_t s1 = p.band > 0 ? 0 : (cta + 1) * p.W / nC;
+  const int n_steps = p.band > 0
+                          ? static_cast<int>(((p.TT * p.F - cta + nC - 1) / nC) * p.G)
+                          : static_cast<int>(s1 - s0);
   const int64_t G = p.G;
   const int64_t F = p.F;
-  const uint64_t pol_w = policy_evict_first();
+  // weights: streamed once (stream-K), or shared by the blocks of a band that
+  // read each tile within microseconds of each other (banded tiles)
+  const uint64_t pol_w = p.band > 0 ? policy_evict_normal() : policy_evict_first();
   const uint64_t pol_a = policy_evict_last();
   int w_issued = 0;   // weight loads issued by the weight producer (warp 0, lane 0)
 
@@ -502,7 +538,7 @@ __global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
     // every TMA load of the SM queues behind the ones issued before it, and
     // the first activation tiles must not wait behind a full weight ring.
     if (p.wtiles == nullptr) prefetch_tmap(&tm_w);
-    StepIter it(s0, G, F);
+    StepIter it(p, s0);
     const int pre = kPreW < stages ? kPreW : stages;
     const int first = n_steps < pre ? n_steps : pre;
     for (int j = 0; j < first; ++j, it.next()) {
@@ -529,7 +565,7 @@ __global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------ weight producer
     if (lane == 0) {
-      StepIter it(s0, G, F);
+      StepIter it(p, s0);
       Ring rg(stages);
       for (int j = 0; j < w_issued; ++j) {
         it.next();
@@ -560,7 +596,7 @@ __global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tm_a);
       if constexpr (C::kScales) prefetch_tmap(&tm_s);
-      StepIter it(s0, G, F);
+      StepIter it(p, s0);
       Ring rg(NXR);
       ChunkIter ch;
       int issued = 0, s_issued = 0;
@@ -630,7 +666,7 @@ __global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
     if (lane == 0) {
       const int me = warp == 1 ? 0 : 1;
       constexpr uint32_t idesc = idesc_f16(kTileF, T, C::kWO);
-      StepIter it(s0, G, F);
+      StepIter it(p, s0);
       Ring rx(NX);
       int seg = 0;
       bool started = false;   // W4A16: this issuer has accumulated into the segment
@@ -700,7 +736,7 @@ __global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
     const int grp = ct >> 7;
     const int r = ct & 127;                                // row of A = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    StepIter it(s0, G, F);
+    StepIter it(p, s0);
     Ring rg(stages);
     Ring ri(C::kXConv ? NXR : 1);   // in-kernel expansion: int8 staging slot of the step
     ChunkIter ch;
@@ -906,7 +942,7 @@ __global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
         }
       }
     };
-    StepIter it(s0, G, F);
+    StepIter it(p, s0);
     ChunkIter ch;
     for (int j = 0; j < n_steps; ++j, it.next(), ch.advance()) {
       const int64_t g = it.g, t = it.t;
@@ -1146,9 +1182,11 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl_in, int* err, cudaStr
   if (GPS > 1) {
     pl.G = pl_in.G / GPS;
     pl.steps = pl.TT * pl.F * pl.G;
-    const int64_t by_work = (pl.steps * GPS + kMinSteps - 1) / kMinSteps;
-    pl.ctas = by_work < pl_in.ctas ? by_work : pl_in.ctas;
-    if (pl.ctas < 1) pl.ctas = 1;
+    if (pl.band == 0) {
+      const int64_t by_work = (pl.steps * GPS + kMinSteps - 1) / kMinSteps;
+      pl.ctas = by_work < pl_in.ctas ? by_work : pl_in.ctas;
+      if (pl.ctas < 1) pl.ctas = 1;
+    }
   }
   const void* act16 = a.act;
   if constexpr (!C::kWO && !C::kXConv) {
@@ -1226,6 +1264,8 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl_in, int* err, cudaStr
   kp.G = pl.G;
   kp.F = pl.F;
   kp.W = pl.steps;
+  kp.TT = pl.TT;
+  kp.band = pl.band;
   kp.counters = static_cast<int*>(a.workspace);
   kp.part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + pl.counter_bytes);
   kp.err = err;
@@ -1278,6 +1318,20 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
   if (p.ctas > static_cast<int64_t>(kArgmaxKeysOffset / sizeof(int)))
     p.ctas = static_cast<int64_t>(kArgmaxKeysOffset / sizeof(int));
   if (p.ctas < 1) p.ctas = 1;
+  // Batches of many token tiles take whole tiles in bands instead (StepIter):
+  // a band's 16-bit activations, about kBandBytes, stay in L2 while every
+  // feature tile passes over them, and the blocks running together share
+  // each weight tile.  No tile is split, so there is no fix-up.
+  p.band = 0;
+  if (p.TT >= kBandMinTiles) {
+    const int64_t tile_bytes = static_cast<int64_t>(p.T) * K * 2;
+    int64_t band = kBandBytes / tile_bytes;
+    if (band < 1) band = 1;
+    if (band > p.TT) band = p.TT;
+    p.band = band;
+    const int64_t tiles = p.TT * p.F;
+    p.ctas = tiles < sm_count ? tiles : sm_count;
+  }
   // One arrival counter per block: a tile split across blocks is counted on
   // the counter of its first contributing block, and a block is the first
   // contributor of at most one split tile (the tile its range ends in).  The

@@ -86,6 +86,7 @@ struct GemmPlan {
   int64_t G;       // groups of 128 along K
   int64_t steps;   // TT * F * G
   int64_t ctas;    // grid size
+  int64_t band;    // banded whole-tile schedule: token tiles per band (0: stream-K)
   size_t counter_bytes;
   size_t act_offset;     // fp16 image of the W8A8 activations (token tiles >= 64)
   size_t workspace_bytes;
