@@ -296,6 +296,10 @@ def _roles(c, st):
             if (j & 1) == grp:
                 ab, abph = j % NB, (j // NB) & 1
                 yield ("wait", f"wfull{j % ST}", (j // ST) & 1)
+                # the weights go to registers first and the slot is released
+                # before the A buffer is waited for
+                yield ("read", f"W{j % ST}")
+                yield ("arrive", f"empty{j % ST}")
                 if ACOMMIT:
                     yield ("wait", f"aempty{ab}", abph ^ 1)
                 elif j >= NB:
@@ -311,10 +315,6 @@ def _roles(c, st):
                 if XC:
                     yield ("read", f"XI{j % NXR}")
                     yield ("write", f"X{ab}")
-                # the weights go to registers first; the slot is released
-                # before they are converted into the A buffer
-                yield ("read", f"W{j % ST}")
-                yield ("arrive", f"empty{j % ST}")
                 yield ("write", f"A{ab}")
                 if XC:
                     yield ("arrive", f"xempty{j % NXR}")

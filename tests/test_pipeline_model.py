@@ -23,8 +23,8 @@ CONFIGS = {
     "W8A16 T16": dict(mode="wo", NB=6, ND=2, stages=7, NX=16),
     "W8A8 T16": dict(mode="w8x", NB=4, ND=16, stages=10, NX=4, NXR=16),
     "W8A8 T32": dict(mode="w8x", NB=4, ND=8, stages=9, NX=4, NXR=8),
-    "W8A8 T64": dict(mode="w8", NB=4, ND=4, stages=9, NX=4),
-    "W8A8 T96": dict(mode="w8", NB=4, ND=2, stages=7, NX=4, EPI=12),
+    "W8A8 T64": dict(mode="w8", NB=2, ND=6, stages=9, NX=4),
+    "W8A8 T96": dict(mode="w8", NB=2, ND=4, stages=7, NX=4, EPI=12),
 }
 
 # (first step, end step, steps per tile): split tiles at both ends, whole

@@ -151,10 +151,13 @@ struct Cfg {
   // W8A8 sizes the A buffers (converter -> MMA) and the D buffers (MMA ->
   // epilogue) separately: the epilogue loop (MMA completion, TMEM drain,
   // release) is the long one, so small token tiles get many D buffers.
-  // 96-token W8A8 tiles keep four A buffers too (two per converter group, so
-  // a group converts its next step while the MMAs read its previous one),
-  // at the price of two D buffers.
-  static constexpr int kNumBufRaw = kWO ? (512 - kW4DCols) / kACols : 4;
+  // Token tiles of 64 and more keep two A buffers (one per converter group)
+  // and give the columns to D buffers: six at 64 tokens, four at 96.  There
+  // the D ring sets the pace (each buffer goes round MMA completion, the
+  // epilogue's wake-up, drain and release, and the issuer's wake-up), while
+  // a converter group loads its next step's weights before it waits for its
+  // A buffer, so only the TMEM stores sit in the A loop.
+  static constexpr int kNumBufRaw = kWO ? (512 - kW4DCols) / kACols : (T <= 32 ? 4 : 2);
   // An even count keeps every A buffer with one converter group and one
   // issuer (steps alternate between the two of each).
   static constexpr int kNumBufCap = kNumBufRaw < 6 ? kNumBufRaw : 6;
@@ -750,7 +753,20 @@ __global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
       if (mine) {
         const int ab = j % NB;
         const uint32_t abph = static_cast<uint32_t>(j / NB) & 1u;
-        bool ok = mbar_wait(smem_u32(&ctrl->wfull[rg.slot]), rg.phase, ctx, 7);
+        if (!warp_all(mbar_wait(smem_u32(&ctrl->wfull[rg.slot]), rg.phase, ctx, 7))) break;
+        // Every word this thread converts in the step, loaded before it waits
+        // for its A buffer (and before the first TMEM store, whose ordering
+        // would otherwise hold each batch of shared-memory loads back behind
+        // the previous batch's conversion); the weight slot is then free for
+        // the next load.
+        const uint32_t* wsm = reinterpret_cast<const uint32_t*>(
+            smem + static_cast<uint32_t>(rg.slot) * C::kStageBytes);
+        uint32_t wreg[C::kWordRows];
+#pragma unroll
+        for (int i = 0; i < C::kWordRows; ++i) wreg[i] = wsm[i * kTileF + r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl->empty[rg.slot]));
+        bool ok = true;
         if constexpr (C::kACommit) {
           if (ok) ok = mbar_wait(smem_u32(&ctrl->a_empty[ab]), abph ^ 1u, ctx, 8);
         } else if (ok && j >= NB) {
@@ -814,18 +830,7 @@ __global__ void __launch_bounds__(Cfg<kMode, T, GPS>::kThreads, 1)
           }
           fence_proxy_async_smem();   // generic writes -> the MMA's async reads
         }
-        const uint32_t* wsm = reinterpret_cast<const uint32_t*>(
-            smem + static_cast<uint32_t>(rg.slot) * C::kStageBytes);
         const uint32_t acol = tmem + lane_off + C::kColA + ab * C::kACols;
-        // Every word this thread converts in the step, loaded before the
-        // first TMEM store (the stores' ordering would otherwise hold each
-        // batch of shared-memory loads back behind the previous batch's
-        // conversion); the weight slot is then free for the next load.
-        uint32_t wreg[C::kWordRows];
-#pragma unroll
-        for (int i = 0; i < C::kWordRows; ++i) wreg[i] = wsm[i * kTileF + r];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctrl->empty[rg.slot]));
 #pragma unroll
         for (int h = 0; h < 4 * GPS; ++h) {
           uint32_t v[16];
