@@ -283,6 +283,14 @@ class LayerRunner:
         weights = {}
         self.inputs = {}
         self.acts = {}
+        # W8A8 inputs of more than 32 rows read only by plain W8A8 GEMMs take
+        # their codes as fp16 (act_quant_c16 -> gemm_w8a8_gs128_c16): the
+        # GEMM's tensor-core operand, with no int8 -> fp16 pass in between
+        self.c16 = {}
+        for spec in specs:
+            ikey = self._ikey(spec)
+            ok = spec[5] == "w8a8" and spec[4] > 32
+            self.c16[ikey] = self.c16.get(ikey, True) and ok
         for name, K, N, kind, M, wk in specs:
             key = (name, wk)
             if key not in weights:
@@ -292,7 +300,8 @@ class LayerRunner:
                 xb = synth.activations(seed, f"{ikey[0]}/M{M}", M, K, kind)
                 self.inputs[ikey] = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(device)
                 if wk.startswith("w8a8"):
-                    self.acts[ikey] = (torch.empty((M, K), dtype=torch.int8, device=device),
+                    cdt = torch.float16 if self.c16[ikey] else torch.int8
+                    self.acts[ikey] = (torch.empty((M, K), dtype=cdt, device=device),
                                        torch.empty((M,), dtype=torch.float32, device=device))
         # calls[fused][copy]: unfused = one call per linear; fused = one call
         # per (input, format)
@@ -375,9 +384,10 @@ class LayerRunner:
 
     def n_launches(self, fused):
         # one kernel per act-quant and per GEMM, plus the int8 -> fp16 operand
-        # pass of W8A8 GEMMs with token tiles of 64 and more (M > 32), plus
-        # the argmax decode
-        return self.n_actq + sum(1 + (c["wk"].startswith("w8a8") and c["M"] > 32)
+        # pass of W8A8 GEMMs with token tiles of 64 and more (M > 32) that
+        # read int8 codes, plus the argmax decode
+        return self.n_actq + sum(1 + (c["wk"].startswith("w8a8") and c["M"] > 32
+                                      and not self.c16[c["ikey"]])
                                  + c["wk"].endswith("_argmax") for c in self.calls[fused][0])
 
     def _ikey(self, spec):
@@ -388,7 +398,10 @@ class LayerRunner:
 
     def quantize(self):
         for ikey, (q, s) in self.acts.items():
-            self.qlin.act_quant_i8(self.inputs[ikey], q, s)
+            if self.c16[ikey]:
+                self.qlin.act_quant_c16(self.inputs[ikey], q, s)
+            else:
+                self.qlin.act_quant_i8(self.inputs[ikey], q, s)
 
     def gemms(self, fused=False, buf=0, copy=0, sel=None):
         ws = self.ws.buf
@@ -401,7 +414,9 @@ class LayerRunner:
                 self.qlin.gemm_w8a8_gs128_argmax(q, s, c["qw"], c["sc"], y, workspace=ws)
             elif c["wk"] == "w8a8":
                 q, s = self.acts[c["ikey"]]
-                self.qlin.gemm_w8a8_gs128(q, s, c["qw"], c["sc"], y, workspace=ws)
+                gemm = (self.qlin.gemm_w8a8_gs128_c16 if self.c16[c["ikey"]]
+                        else self.qlin.gemm_w8a8_gs128)
+                gemm(q, s, c["qw"], c["sc"], y, workspace=ws)
             elif c["wk"] == "w8a16":
                 self.qlin.gemm_w8a16(self.inputs[c["ikey"]], c["qw"], c["sc"], W8A16_GROUP, y,
                                      workspace=ws)

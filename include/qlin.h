@@ -132,6 +132,29 @@ qlin_status_t qlin_silu_mul_act_quant_i8(const uint16_t *gate_up, int64_t M, int
                                          qlin_stream_t stream);
 
 /*
+ * The three producers above with the codes written as fp16 instead of int8:
+ * q[m,k] is the same integer in [-127, 127], stored as its (exact) fp16 value,
+ * fp16 [M, K] (or [M, I]).  s_a and y as above.
+ *
+ * The passages are those of the producers above; the width of the codes is
+ * a storage choice of this library.  qlin_gemm_w8a8_gs128_c16 reads these
+ * codes: for batches of more than 32 tokens its tensor-core operands are the
+ * fp16 codes themselves, so handing them over directly saves the conversion
+ * pass that the int8 entry runs first.  The results are bit-identical to the
+ * int8 pair (qlin_*_i8 followed by qlin_gemm_w8a8_gs128).
+ */
+qlin_status_t qlin_act_quant_c16(const uint16_t *x, int64_t M, int64_t K,
+                                 uint16_t *q, float *s_a, qlin_stream_t stream);
+
+qlin_status_t qlin_rmsnorm_act_quant_c16(const uint16_t *x, const uint16_t *gamma, float eps,
+                                         int64_t M, int64_t K, uint16_t *q, float *s_a,
+                                         uint16_t *y, qlin_stream_t stream);
+
+qlin_status_t qlin_silu_mul_act_quant_c16(const uint16_t *gate_up, int64_t M, int64_t I,
+                                          uint16_t *q, float *s_a, uint16_t *y,
+                                          qlin_stream_t stream);
+
+/*
  * W8A8 GS128 linear:  y = bf16( s_a[m] * sum_g s_w[g,n] * P[g,m,n] ),
  * P[g,m,n] = sum_{k = 128g}^{128g+127} q_a[m,k] * q_w[k,n]  (exact integers).
  *
@@ -164,6 +187,19 @@ qlin_status_t qlin_gemm_w8a8_gs128(const int8_t *q_a, const float *s_a,
                                    int64_t M, int64_t N, int64_t K, uint16_t *y,
                                    void *workspace, size_t workspace_bytes,
                                    qlin_stream_t stream);
+
+/*
+ * qlin_gemm_w8a8_gs128 with the activation codes as fp16 (the output of the
+ * qlin_*_c16 producers): q_a fp16 [M, K], every value an integer in
+ * [-127, 127]; other values are outside the contract.  Same results, same
+ * workspace size.  Batches of up to 32 tokens, whose kernel reads int8
+ * codes, first narrow the codes into the workspace.
+ */
+qlin_status_t qlin_gemm_w8a8_gs128_c16(const uint16_t *q_a, const float *s_a,
+                                       const int32_t *qweight, const uint16_t *scales,
+                                       int64_t M, int64_t N, int64_t K, uint16_t *y,
+                                       void *workspace, size_t workspace_bytes,
+                                       qlin_stream_t stream);
 
 /*
  * W8A8 GS128 linear for callers that cannot allocate device memory.
@@ -412,7 +448,10 @@ const char *qlin_status_string(qlin_status_t status);
  * changed, except that an empty batch (M == 0) now accepts NULL batch
  * buffers.  1.2 (102) adds the tile layout (qlin_tiles_bytes,
  * qlin_pack_tiles) and the tiled W8A8 and W4A16 GEMMs; the greedy-argmax
- * calls now take at most 96 rows. */
+ * calls now take at most 96 rows.  1.3 (103) adds the fp16 activation codes
+ * (qlin_act_quant_c16, qlin_rmsnorm_act_quant_c16,
+ * qlin_silu_mul_act_quant_c16, qlin_gemm_w8a8_gs128_c16); the workspace of
+ * batches of up to 32 tokens grows by M * K bytes. */
 int qlin_version(void);
 
 #ifdef __cplusplus

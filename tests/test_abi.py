@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert qlin.version() == 102
+    assert qlin.version() == 103
     codes = [0, -1, -2, -3, -4, -5, -6, -7, -10, -20, -21]
     names = [qlin.status_string(c) for c in codes]
     assert len(set(names)) == len(codes)

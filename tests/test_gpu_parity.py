@@ -689,3 +689,125 @@ def test_banded_tile_schedule_w4a16(M, K, N):
     rows = np.concatenate([np.arange(0, M, 7), [M - 1]])
     ref = oracle.gemm_w4a16_g128(xb, qw, sb, K, rows)
     compare_linear(np.ascontiguousarray(y[rows]), ref, f"banded w4a16 {M}x{K}x{N}", "w4a16", K)
+
+
+# -------------------------------------------- activation codes stored as fp16
+
+def _codes_as_i8(q16):
+    """fp16 codes -> int8, asserting that every code is an integer in range."""
+    f = q16.float().cpu().numpy()
+    assert np.array_equal(f, np.rint(f)) and np.abs(f).max(initial=0) <= 127
+    return f.astype(np.int8)
+
+
+@pytest.mark.parametrize("M,K,kind", [(1, 128, "normal"), (8, 5120, "outliers"), (33, 4096, "normal2"),
+                                      (96, 17408, "silu_mul"), (300, 1280, "outliers"),
+                                      (4, 33024, "outliers")])
+def test_act_quant_c16_holds_the_int8_codes(M, K, kind):
+    xb = synth.activations(40, f"gpu/aq16/{M}/{K}", M, K, kind)
+    if M > 2:
+        xb[1, :] = 0                     # an all-zero row
+    x = to_dev_bits(xb, torch.bfloat16)
+    q16, s16 = qlin.act_quant_c16(x)
+    torch.cuda.synchronize()
+    oq, os_ = oracle.act_quant_i8(xb)
+    assert np.array_equal(_codes_as_i8(q16), oq)
+    assert np.array_equal(s16.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (64, 5120), (130, 640), (3, 40960)])
+def test_rmsnorm_act_quant_c16_holds_the_int8_codes(M, K):
+    x = synth.activations(41, f"gpu/rms16/{M}/{K}", M, K, "outliers")
+    g = synth.bf16_bits(1.0 + 0.1 * synth.normal(41, f"gpu/rms16/{K}/gamma", (K,)))
+    xd, gd = to_dev_bits(x, torch.bfloat16), to_dev_bits(g, torch.bfloat16)
+    y = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    q16, s16 = qlin.rmsnorm_act_quant_c16(xd, gd, 1e-6, y=y)
+    q8, s8 = qlin.rmsnorm_act_quant_i8(xd, gd, 1e-6)
+    torch.cuda.synchronize()
+    q_ref, s_ref, z_ref = oracle.rmsnorm_act_quant_i8(x, g, 1e-6)
+    assert np.array_equal(_codes_as_i8(q16), q_ref)
+    assert np.array_equal(q8.cpu().numpy(), q_ref)
+    assert np.array_equal(s16.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert torch.equal(s16, s8)
+    assert np.array_equal(from_dev_bits(y), z_ref)
+
+
+@pytest.mark.parametrize("M,I", [(1, 128), (96, 17408), (130, 384), (2, 34816)])
+def test_silu_mul_act_quant_c16_holds_the_int8_codes(M, I):
+    gu = synth.activations(42, f"gpu/silu16/{M}/{I}", M, 2 * I, "normal2")
+    gud = to_dev_bits(gu, torch.bfloat16)
+    q16, s16 = qlin.silu_mul_act_quant_c16(gud)
+    q8, s8 = qlin.silu_mul_act_quant_i8(gud)
+    torch.cuda.synchronize()
+    q_ref, s_ref, _ = oracle.silu_mul_act_quant_i8(gu)
+    assert np.array_equal(_codes_as_i8(q16), q_ref)
+    assert np.array_equal(q8.cpu().numpy(), q_ref)
+    assert torch.equal(s16, s8)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 256, 136), (8, 5120, 1024), (17, 640, 264), (32, 1280, 776),
+                                   (33, 384, 200), (64, 4096, 512), (65, 640, 264), (96, 2560, 776),
+                                   (130, 512, 256), (600, 384, 776), (8, 128, 40960)])
+def test_gemm_w8a8_c16_equals_int8_call(M, K, N):
+    """The fp16-code entry computes what the int8 entry computes, bit for
+    bit, on every token-tile size: 16 and 32 (codes narrowed to int8 in the
+    workspace), 64 and 96 (the codes are the tensor-core operand), the banded
+    schedule (600 rows), and so within the tolerance of the oracle."""
+    _, qa, sa, _, qw, swb = _w8a8_inputs(43, f"gpu/c16/{M}/{K}/{N}", M, K, N)
+    qad, sad = to_dev(qa), to_dev(sa)
+    q16 = qad.to(torch.float16)            # exact: every int8 value is an fp16 integer
+    sc, qwd = to_dev_bits(swb, torch.float16), to_dev(qw)
+    y8 = qlin.gemm_w8a8_gs128(qad, sad, qwd, sc)
+    y16 = qlin.gemm_w8a8_gs128_c16(q16, sad, qwd, sc)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev_bits(y16), from_dev_bits(y8))
+    rows = np.arange(M) if M <= 130 else np.concatenate([np.arange(0, M, 7), [M - 1]])
+    ref = oracle.gemm_w8a8_gs128(qa, sa, qw, swb, K, rows if M > 130 else None)
+    got = from_dev_bits(y16)
+    compare_linear(np.ascontiguousarray(got[rows]) if M > 130 else got, ref,
+                   f"w8a8 c16 {M}x{K}x{N}")
+
+
+def test_c16_chain_equals_int8_chain():
+    """Producer -> GEMM through fp16 codes gives the int8 chain's output bit
+    for bit (norm -> q/k/v-like GEMM at 96 tokens, SiLU -> down-like GEMM at
+    8 tokens)."""
+    M, K, N = 96, 1280, 512
+    x = synth.activations(44, "gpu/chain16/x", M, K, "outliers")
+    g = synth.bf16_bits(1.0 + 0.1 * synth.normal(44, "gpu/chain16/g", (K,)))
+    _, _, _, _, qw, swb = _w8a8_inputs(44, "gpu/chain16/w", 1, K, N)
+    xd, gd = to_dev_bits(x, torch.bfloat16), to_dev_bits(g, torch.bfloat16)
+    sc, qwd = to_dev_bits(swb, torch.float16), to_dev(qw)
+    a8 = qlin.gemm_w8a8_gs128(*qlin.rmsnorm_act_quant_i8(xd, gd, 1e-6), qwd, sc)
+    a16 = qlin.gemm_w8a8_gs128_c16(*qlin.rmsnorm_act_quant_c16(xd, gd, 1e-6), qwd, sc)
+    gu = to_dev_bits(synth.activations(44, "gpu/chain16/gu", 8, 2 * K, "normal2"), torch.bfloat16)
+    b8 = qlin.gemm_w8a8_gs128(*qlin.silu_mul_act_quant_i8(gu), qwd, sc)
+    b16 = qlin.gemm_w8a8_gs128_c16(*qlin.silu_mul_act_quant_c16(gu), qwd, sc)
+    torch.cuda.synchronize()
+    assert torch.equal(a8, a16) and torch.equal(b8, b16)
+
+
+def test_c16_empty_batch_and_bad_arguments():
+    K, N, dev = 256, 128, "cuda"
+    x = torch.empty((0, K), dtype=torch.bfloat16, device=dev)
+    q, s = qlin.act_quant_c16(x)
+    assert q.shape == (0, K) and q.dtype == torch.float16
+    g = torch.ones((K,), dtype=torch.bfloat16, device=dev)
+    assert qlin.rmsnorm_act_quant_c16(x, g, 1e-6)[0].shape == (0, K)
+    assert qlin.silu_mul_act_quant_c16(torch.empty((0, 2 * K), dtype=torch.bfloat16,
+                                                   device=dev))[0].shape == (0, K)
+    qw8 = torch.zeros((K // 4, N), dtype=torch.int32, device=dev)
+    s16 = torch.ones((K // 128, N), dtype=torch.float16, device=dev)
+    assert qlin.gemm_w8a8_gs128_c16(torch.empty((0, K), dtype=torch.float16, device=dev),
+                                    torch.empty((0,), dtype=torch.float32, device=dev),
+                                    qw8, s16).shape == (0, N)
+    lib = qlin.load()
+    # K not a multiple of 128; a misaligned code pointer
+    assert lib.qlin_act_quant_c16(None, 0, 200, None, None, None) == qlin.QLIN_ERR_SHAPE
+    xa = torch.zeros((2, K), dtype=torch.bfloat16, device=dev)
+    qb = torch.zeros((2 * K + 8,), dtype=torch.float16, device=dev)
+    sb = torch.zeros((2,), dtype=torch.float32, device=dev)
+    assert lib.qlin_act_quant_c16(xa.data_ptr(), 2, K, qb.data_ptr() + 2, sb.data_ptr(),
+                                  None) == qlin.QLIN_ERR_ALIGN
+    torch.cuda.synchronize()
+    assert qlin.device_status() == qlin.QLIN_OK

@@ -81,12 +81,34 @@ __device__ __forceinline__ uint2 quant8y(uint4 v, float s, float y) {
   return o;
 }
 
+// The codes of one row: int8, or (c16) the same integers as fp16 values,
+// which the W8A8 GEMM's tensor cores read without a conversion pass.
+// Each store takes 8 consecutive codes (element 8v .. 8v + 7 of the row).
+struct CodeRow {
+  void* base;
+  bool c16;
+  __device__ __forceinline__ CodeRow(void* q, int64_t row_elems, int64_t m, bool c16_)
+      : base(c16_ ? static_cast<void*>(static_cast<uint16_t*>(q) + m * row_elems)
+                  : static_cast<void*>(static_cast<int8_t*>(q) + m * row_elems)),
+        c16(c16_) {}
+  __device__ __forceinline__ void store(int64_t v, uint2 codes) const {
+    if (!c16) {
+      reinterpret_cast<uint2*>(base)[v] = codes;
+    } else {
+      uint4 o;
+      biased_u8x4_to_f16x4(codes.x ^ 0x80808080u, o.x, o.y);
+      biased_u8x4_to_f16x4(codes.y ^ 0x80808080u, o.z, o.w);
+      reinterpret_cast<uint4*>(base)[v] = o;
+    }
+  }
+};
+
 // kThreads threads per row: 1024 for small batches (each row's latency is the
 // whole call's), 256 for many rows (several blocks per SM).
 template <bool kCached, int kThreads>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __restrict__ x,
-                                                             int64_t K, int8_t* __restrict__ q,
-                                                             float* __restrict__ s_out) {
+                                                             int64_t K, void* __restrict__ q,
+                                                             float* __restrict__ s_out, bool c16) {
   constexpr int kVec = kAqRowVecs / kThreads;
   __shared__ float red[kThreads / 32];
   // Launched with programmatic serialization: wait for the previous kernel
@@ -97,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
   const int64_t m = blockIdx.x;
   const int64_t nvec = K / 8;
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
-  uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
+  const CodeRow qrow(q, K, m, c16);
   const int tid = threadIdx.x;
 
   uint4 cache[kCached ? kVec : 1];
@@ -125,7 +147,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
   const float s = __fdiv_rn(amax, 127.0f);
   if (tid == 0) s_out[m] = s;
   if (amax == 0.0f) {
-    for (int64_t v = tid; v < nvec; v += kThreads) qrow[v] = make_uint2(0u, 0u);
+    for (int64_t v = tid; v < nvec; v += kThreads) qrow.store(v, make_uint2(0u, 0u));
     return;
   }
   const float y = __frcp_rn(s);
@@ -133,10 +155,10 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
       const int64_t v = tid + static_cast<int64_t>(i) * kThreads;
-      if (v < nvec) qrow[v] = quant8y(cache[i], s, y);
+      if (v < nvec) qrow.store(v, quant8y(cache[i], s, y));
     }
   } else {
-    for (int64_t v = tid; v < nvec; v += kThreads) qrow[v] = quant8y(__ldg(row + v), s, y);
+    for (int64_t v = tid; v < nvec; v += kThreads) qrow.store(v, quant8y(__ldg(row + v), s, y));
   }
 }
 
@@ -309,7 +331,7 @@ __device__ __forceinline__ RowScale block_row_scale(float s, float c, float2* re
 // row), z, then act-quant of z.
 __global__ void __launch_bounds__(kAqThreads) rmsnorm_quant_long_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps, int64_t K,
-    int8_t* __restrict__ q, float* __restrict__ s_out, uint16_t* __restrict__ y) {
+    void* __restrict__ q, float* __restrict__ s_out, uint16_t* __restrict__ y, bool c16) {
   __shared__ float red[kAqThreads / 32];
   __shared__ float2 red2[kAqThreads / 32];
   __shared__ RowScale row_rs;
@@ -319,7 +341,7 @@ __global__ void __launch_bounds__(kAqThreads) rmsnorm_quant_long_kernel(
   const int64_t nvec = K / 8;
   const uint4* row = reinterpret_cast<const uint4*>(x + m * K);
   const uint4* grow = reinterpret_cast<const uint4*>(gamma);
-  uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
+  const CodeRow qrow(q, K, m, c16);
   uint4* yrow = y ? reinterpret_cast<uint4*>(y + m * K) : nullptr;
   const int tid = threadIdx.x;
   float ss = 0.0f, sc = 0.0f;
@@ -335,14 +357,14 @@ __global__ void __launch_bounds__(kAqThreads) rmsnorm_quant_long_kernel(
   const float s = __fdiv_rn(amax, 127.0f);
   if (tid == 0) s_out[m] = s;
   for (int64_t v = tid; v < nvec; v += kAqThreads)
-    qrow[v] = amax == 0.0f ? make_uint2(0u, 0u)
-                           : quant8(norm8(__ldg(row + v), __ldg(grow + v), rstd), s);
+    qrow.store(v, amax == 0.0f ? make_uint2(0u, 0u)
+                               : quant8(norm8(__ldg(row + v), __ldg(grow + v), rstd), s));
 }
 
 // The same for SiLU(gate) * up rows of more than 32768 elements.
 __global__ void __launch_bounds__(kAqThreads) silu_mul_quant_long_kernel(
-    const uint16_t* __restrict__ gate_up, int64_t I, int8_t* __restrict__ q,
-    float* __restrict__ s_out, uint16_t* __restrict__ y) {
+    const uint16_t* __restrict__ gate_up, int64_t I, void* __restrict__ q,
+    float* __restrict__ s_out, uint16_t* __restrict__ y, bool c16) {
   __shared__ float red[kAqThreads / 32];
   grid_dep_wait();
   grid_dep_launch();
@@ -350,7 +372,7 @@ __global__ void __launch_bounds__(kAqThreads) silu_mul_quant_long_kernel(
   const int64_t nvec = I / 8;
   const uint4* grow = reinterpret_cast<const uint4*>(gate_up + m * 2 * I);
   const uint4* urow = grow + nvec;
-  uint2* qrow = reinterpret_cast<uint2*>(q + m * I);
+  const CodeRow qrow(q, I, m, c16);
   uint4* yrow = y ? reinterpret_cast<uint4*>(y + m * I) : nullptr;
   const int tid = threadIdx.x;
   float amax = 0.0f;
@@ -363,7 +385,8 @@ __global__ void __launch_bounds__(kAqThreads) silu_mul_quant_long_kernel(
   const float s = __fdiv_rn(amax, 127.0f);
   if (tid == 0) s_out[m] = s;
   for (int64_t v = tid; v < nvec; v += kAqThreads)
-    qrow[v] = amax == 0.0f ? make_uint2(0u, 0u) : quant8(silu_mul8(__ldg(grow + v), __ldg(urow + v)), s);
+    qrow.store(v, amax == 0.0f ? make_uint2(0u, 0u)
+                               : quant8(silu_mul8(__ldg(grow + v), __ldg(urow + v)), s));
 }
 
 // Persistent form for rows that fit on chip (up to 32768 elements): blocks of
@@ -385,13 +408,14 @@ struct ProducerParams {
   const uint16_t* gamma;   // norm weight [K]
   float eps;
   int64_t M, K;            // K: elements of one quantized row
-  int8_t* q;
+  void* q;                 // int8 codes, or fp16 codes when c16
   float* s;
   uint16_t* y;             // optional bf16 producer output
   int* err;
   uint64_t limit_ns;
   int stages;
   uint32_t row_bytes;      // input bytes of one row
+  bool c16;
 };
 
 template <int kThreads>
@@ -500,13 +524,13 @@ __global__ void __launch_bounds__(kPThreads) producer_quant_kernel(const Produce
     const float s = __fdiv_rn(amax, 127.0f);
     const float y = __frcp_rn(s);
     if (tid == 0) p.s[m] = s;
-    uint2* qrow = reinterpret_cast<uint2*>(p.q + m * p.K);
+    const CodeRow qrow(p.q, p.K, m, p.c16);
     uint4* yrow = p.y ? reinterpret_cast<uint4*>(p.y + m * p.K) : nullptr;
 #pragma unroll
     for (int j = 0; j < kPVec; ++j) {
       const int64_t v = tid + static_cast<int64_t>(j) * kPThreads;
       if (v < nvec) {
-        qrow[v] = amax == 0.0f ? make_uint2(0u, 0u) : quant8y(z[j], s, y);
+        qrow.store(v, amax == 0.0f ? make_uint2(0u, 0u) : quant8y(z[j], s, y));
         if (yrow) yrow[v] = z[j];
       }
     }
@@ -567,36 +591,39 @@ bool launch_producer(const ProducerParams& pp, int sm_count, cudaStream_t stream
 }  // namespace
 
 cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
-                                 int64_t K, int8_t* q, float* s, uint16_t* y, int* err,
+                                 int64_t K, void* q, bool c16, float* s, uint16_t* y, int* err,
                                  int sm_count, cudaStream_t stream) {
   const ProducerParams pp{x, gamma, eps, M, K, q, s, y, err, 0, 0,
-                          static_cast<uint32_t>(K * 2)};
+                          static_cast<uint32_t>(K * 2), c16};
   cudaError_t e = cudaSuccess;
   if (K <= 32768 && launch_producer<kProdRms>(pp, sm_count, stream, &e)) return e;
   return launch_pdl(rmsnorm_quant_long_kernel, dim3(static_cast<unsigned>(M)), dim3(kAqThreads), 0,
-                    stream, x, gamma, eps, K, q, s, y);
+                    stream, x, gamma, eps, K, q, s, y, c16);
 }
 
-cudaError_t launch_silu_mul_quant(const uint16_t* gate_up, int64_t M, int64_t I, int8_t* q,
-                                  float* s, uint16_t* y, int* err, int sm_count,
+cudaError_t launch_silu_mul_quant(const uint16_t* gate_up, int64_t M, int64_t I, void* q,
+                                  bool c16, float* s, uint16_t* y, int* err, int sm_count,
                                   cudaStream_t stream) {
   const ProducerParams pp{gate_up, nullptr, 0.0f, M, I, q, s, y, err, 0, 0,
-                          static_cast<uint32_t>(I * 4)};
+                          static_cast<uint32_t>(I * 4), c16};
   cudaError_t e = cudaSuccess;
   if (I <= 32768 && launch_producer<kProdSilu>(pp, sm_count, stream, &e)) return e;
   return launch_pdl(silu_mul_quant_long_kernel, dim3(static_cast<unsigned>(M)), dim3(kAqThreads), 0,
-                    stream, gate_up, I, q, s, y);
+                    stream, gate_up, I, q, s, y, c16);
 }
 
-cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s,
-                             cudaStream_t stream) {
+cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, void* q, bool c16,
+                             float* s, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(M));
   const bool cached = K <= static_cast<int64_t>(kAqRowVecs) * 8;
   if (M <= 256)
-    return cached ? launch_pdl(act_quant_kernel<true, 1024>, grid, dim3(1024), 0, stream, x, K, q, s)
-                  : launch_pdl(act_quant_kernel<false, 1024>, grid, dim3(1024), 0, stream, x, K, q, s);
-  return cached ? launch_pdl(act_quant_kernel<true, 256>, grid, dim3(256), 0, stream, x, K, q, s)
-                : launch_pdl(act_quant_kernel<false, 256>, grid, dim3(256), 0, stream, x, K, q, s);
+    return cached ? launch_pdl(act_quant_kernel<true, 1024>, grid, dim3(1024), 0, stream, x, K, q,
+                               s, c16)
+                  : launch_pdl(act_quant_kernel<false, 1024>, grid, dim3(1024), 0, stream, x, K, q,
+                               s, c16);
+  return cached ? launch_pdl(act_quant_kernel<true, 256>, grid, dim3(256), 0, stream, x, K, q, s, c16)
+                : launch_pdl(act_quant_kernel<false, 256>, grid, dim3(256), 0, stream, x, K, q, s,
+                             c16);
 }
 
 }  // namespace qlin

@@ -1114,6 +1114,29 @@ __global__ void __launch_bounds__(256) act_i8_to_f16_kernel(const int8_t* __rest
   }
 }
 
+// fp16 codes -> int8 codes (exact: the values are integers in [-127, 127]),
+// 8 per thread: the int8 input of the W8A8 GEMM at token tiles of 32 and
+// fewer, which expand int8 tiles themselves.  Ordered like the kernel above.
+__global__ void __launch_bounds__(256) act_f16_to_i8_kernel(const uint16_t* __restrict__ c,
+                                                            int8_t* __restrict__ out,
+                                                            int64_t n8) {
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 h = __ldg(reinterpret_cast<const uint4*>(c) + i);
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+    uint32_t b[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint16_t bits = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+      const int v = __half2int_rn(__ushort_as_half(bits));
+      b[j >> 2] |= (static_cast<uint32_t>(v) & 0xFFu) << (8 * (j & 3));
+    }
+    reinterpret_cast<uint2*>(out)[i] = make_uint2(b[0], b[1]);
+  }
+}
+
 // Greedy argmax: the column index encoded in each row's key.
 __global__ void __launch_bounds__(128) argmax_finalize_kernel(const unsigned long long* keys,
                                                               int64_t M, int32_t* idx) {
@@ -1193,17 +1216,34 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl_in, int* err, cudaStr
       if (pl.ctas < 1) pl.ctas = 1;
     }
   }
-  const void* act16 = a.act;
+  const void* act16 = a.act;   // 16-bit activation tiles (TMA)
+  const void* act8 = a.act;    // int8 activation tiles (in-kernel expansion)
+  if constexpr (C::kXConv) {
+    if (a.act_c16) {
+      // fp16 codes -> int8 codes in the workspace
+      int8_t* dst = static_cast<int8_t*>(a.workspace) + pl.act_offset;
+      const int64_t n8 = a.M * a.K / 8;
+      int64_t blocks = (n8 + 255) / 256;
+      if (blocks > 4096) blocks = 4096;
+      cudaError_t e = launch_pdl(act_f16_to_i8_kernel, dim3(static_cast<unsigned>(blocks)),
+                                 dim3(256), 0, stream, static_cast<const uint16_t*>(a.act), dst, n8);
+      if (e != cudaSuccess) return e;
+      act8 = dst;
+    }
+  }
   if constexpr (!C::kWO && !C::kXConv) {
-    // int8 activations -> fp16 image in the workspace
-    uint16_t* dst = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.workspace) + pl.act_offset);
-    const int64_t n16 = a.M * a.K / 16;
-    int64_t blocks = (n16 + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    cudaError_t e = launch_pdl(act_i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256),
-                               0, stream, static_cast<const int8_t*>(a.act), dst, n16);
-    if (e != cudaSuccess) return e;
-    act16 = dst;
+    if (!a.act_c16) {
+      // int8 codes -> fp16 image in the workspace
+      uint16_t* dst =
+          reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.workspace) + pl.act_offset);
+      const int64_t n16 = a.M * a.K / 16;
+      int64_t blocks = (n16 + 255) / 256;
+      if (blocks > 4096) blocks = 4096;
+      cudaError_t e = launch_pdl(act_i8_to_f16_kernel, dim3(static_cast<unsigned>(blocks)),
+                                 dim3(256), 0, stream, static_cast<const int8_t*>(a.act), dst, n16);
+      if (e != cudaSuccess) return e;
+      act16 = dst;
+    }
   }
   CUtensorMap tw, ta;
   const uint64_t words_rows = static_cast<uint64_t>(a.K) / (C::kInt4 ? 8 : 4);
@@ -1220,7 +1260,7 @@ cudaError_t launch_t(const GemmArgs& a, const GemmPlan& pl_in, int* err, cudaStr
       return cudaErrorInvalidValue;
   } else {
     // int8 q_a [M][K]: one box is a 128-wide group of T rows, 128-byte swizzled
-    if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.act, a.K, a.M, a.K, kGroup, T,
+    if (!make_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, act8, a.K, a.M, a.K, kGroup, T,
                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -1344,11 +1384,12 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int sm_count) {
   // any shape that share a workspace never see each other's partials there.
   p.counter_bytes = kCounterBytes;
   const size_t partial_bytes = static_cast<size_t>(p.ctas) * 2 * p.T * kTileF * sizeof(float);
-  // then, for token tiles of 64 and more, the fp16 image of the W8A8
-  // activations (1 KB aligned)
+  // then the W8A8 activations in the code width the kernel reads, when the
+  // caller's is the other one (1 KB aligned): the fp16 image of int8 codes
+  // for token tiles of 64 and more, the int8 codes of fp16 ones below
   p.act_offset = (p.counter_bytes + partial_bytes + 1023) & ~static_cast<size_t>(1023);
-  p.workspace_bytes = p.T >= 64 ? p.act_offset + static_cast<size_t>(M) * static_cast<size_t>(K) * 2
-                                : p.counter_bytes + partial_bytes;
+  p.workspace_bytes = p.act_offset +
+                      static_cast<size_t>(M) * static_cast<size_t>(K) * (p.T >= 64 ? 2 : 1);
   return p;
 }
 

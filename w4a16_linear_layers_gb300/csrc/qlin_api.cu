@@ -81,7 +81,7 @@ qlin_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLI
 qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const int32_t* qweight,
                        const uint16_t* scales, void* out, int64_t M, int64_t N, int64_t K,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                       int group_size = 128, bool tiled = false) {
+                       int group_size = 128, bool tiled = false, bool act_c16 = false) {
   // an empty batch reads and writes nothing: its activation, scale and
   // output pointers may be NULL.  `tiled`: qweight holds the tile layout.
   const bool rows = M != 0;
@@ -103,6 +103,7 @@ qlin_status_t run_gemm(GemmMode mode, const void* act, const float* s_a, const i
   GemmArgs a{mode, act, s_a, qweight, scales, out, M, N, K, workspace, workspace_bytes};
   a.group_size = group_size;
   if (tiled) a.wtiles = qweight;
+  a.act_c16 = act_c16;
   return from_cuda(launch_gemm(a, plan, d->err_word, stream));
 }
 
@@ -140,12 +141,9 @@ qlin_status_t run_argmax(GemmMode mode, const void* act, const float* s_a, const
   return from_cuda(launch_argmax_finalize(keys, M, idx, stream));
 }
 
-}  // namespace
 
-extern "C" {
-
-qlin_status_t qlin_act_quant_i8(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s_a,
-                                qlin_stream_t stream) {
+qlin_status_t run_act_quant(const uint16_t* x, int64_t M, int64_t K, void* q, bool c16,
+                            float* s_a, cudaStream_t stream) {
   if (M != 0 && (x == nullptr || q == nullptr || s_a == nullptr)) return QLIN_ERR_NULL;
   if (M < 0 || M > kMaxDim || K < kGroup || K > kMaxDim || (K % kGroup) != 0)
     return QLIN_ERR_SHAPE;
@@ -154,12 +152,12 @@ qlin_status_t qlin_act_quant_i8(const uint16_t* x, int64_t M, int64_t K, int8_t*
   qlin_status_t st = device_or_error(&d);
   if (st != QLIN_OK) return st;
   if (M == 0) return QLIN_OK;
-  return from_cuda(launch_act_quant(x, M, K, q, s_a, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_act_quant(x, M, K, q, c16, s_a, stream));
 }
 
-qlin_status_t qlin_rmsnorm_act_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps,
-                                        int64_t M, int64_t K, int8_t* q, float* s_a, uint16_t* y,
-                                        qlin_stream_t stream) {
+qlin_status_t run_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
+                                int64_t K, void* q, bool c16, float* s_a, uint16_t* y,
+                                cudaStream_t stream) {
   if (gamma == nullptr || (M != 0 && (x == nullptr || q == nullptr || s_a == nullptr)))
     return QLIN_ERR_NULL;
   if (M < 0 || M > kMaxDim || K < kGroup || K > kMaxDim || (K % kGroup) != 0 || !(eps >= 0.0f) ||
@@ -172,12 +170,12 @@ qlin_status_t qlin_rmsnorm_act_quant_i8(const uint16_t* x, const uint16_t* gamma
   qlin_status_t st = device_or_error(&d);
   if (st != QLIN_OK) return st;
   if (M == 0) return QLIN_OK;
-  return from_cuda(launch_rmsnorm_quant(x, gamma, eps, M, K, q, s_a, y, d->err_word, d->sm_count,
-                                        reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(
+      launch_rmsnorm_quant(x, gamma, eps, M, K, q, c16, s_a, y, d->err_word, d->sm_count, stream));
 }
 
-qlin_status_t qlin_silu_mul_act_quant_i8(const uint16_t* gate_up, int64_t M, int64_t I, int8_t* q,
-                                         float* s_a, uint16_t* y, qlin_stream_t stream) {
+qlin_status_t run_silu_mul_quant(const uint16_t* gate_up, int64_t M, int64_t I, void* q, bool c16,
+                                 float* s_a, uint16_t* y, cudaStream_t stream) {
   if (M != 0 && (gate_up == nullptr || q == nullptr || s_a == nullptr)) return QLIN_ERR_NULL;
   if (M < 0 || M > kMaxDim || I < kGroup || I > kMaxDim || (I % kGroup) != 0)
     return QLIN_ERR_SHAPE;
@@ -187,8 +185,49 @@ qlin_status_t qlin_silu_mul_act_quant_i8(const uint16_t* gate_up, int64_t M, int
   qlin_status_t st = device_or_error(&d);
   if (st != QLIN_OK) return st;
   if (M == 0) return QLIN_OK;
-  return from_cuda(launch_silu_mul_quant(gate_up, M, I, q, s_a, y, d->err_word, d->sm_count,
-                                         reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(
+      launch_silu_mul_quant(gate_up, M, I, q, c16, s_a, y, d->err_word, d->sm_count, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+qlin_status_t qlin_act_quant_i8(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s_a,
+                                qlin_stream_t stream) {
+  return run_act_quant(x, M, K, q, false, s_a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_act_quant_c16(const uint16_t* x, int64_t M, int64_t K, uint16_t* q,
+                                 float* s_a, qlin_stream_t stream) {
+  return run_act_quant(x, M, K, q, true, s_a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_rmsnorm_act_quant_i8(const uint16_t* x, const uint16_t* gamma, float eps,
+                                        int64_t M, int64_t K, int8_t* q, float* s_a, uint16_t* y,
+                                        qlin_stream_t stream) {
+  return run_rmsnorm_quant(x, gamma, eps, M, K, q, false, s_a, y,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_rmsnorm_act_quant_c16(const uint16_t* x, const uint16_t* gamma, float eps,
+                                         int64_t M, int64_t K, uint16_t* q, float* s_a,
+                                         uint16_t* y, qlin_stream_t stream) {
+  return run_rmsnorm_quant(x, gamma, eps, M, K, q, true, s_a, y,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_silu_mul_act_quant_i8(const uint16_t* gate_up, int64_t M, int64_t I, int8_t* q,
+                                         float* s_a, uint16_t* y, qlin_stream_t stream) {
+  return run_silu_mul_quant(gate_up, M, I, q, false, s_a, y,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_silu_mul_act_quant_c16(const uint16_t* gate_up, int64_t M, int64_t I,
+                                          uint16_t* q, float* s_a, uint16_t* y,
+                                          qlin_stream_t stream) {
+  return run_silu_mul_quant(gate_up, M, I, q, true, s_a, y,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 qlin_status_t qlin_gemm_w8a8_gs128(const int8_t* q_a, const float* s_a, const int32_t* qweight,
@@ -197,6 +236,14 @@ qlin_status_t qlin_gemm_w8a8_gs128(const int8_t* q_a, const float* s_a, const in
                                    qlin_stream_t stream) {
   return run_gemm(GemmMode::kW8A8, q_a, s_a, qweight, scales, y, M, N, K, workspace,
                   workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status_t qlin_gemm_w8a8_gs128_c16(const uint16_t* q_a, const float* s_a,
+                                       const int32_t* qweight, const uint16_t* scales, int64_t M,
+                                       int64_t N, int64_t K, uint16_t* y, void* workspace,
+                                       size_t workspace_bytes, qlin_stream_t stream) {
+  return run_gemm(GemmMode::kW8A8, q_a, s_a, qweight, scales, y, M, N, K, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream), 128, false, true);
 }
 
 qlin_status_t qlin_gemm_w8a8_gs128_tiled(const int8_t* q_a, const float* s_a, const int32_t* tiles,
@@ -376,6 +423,6 @@ const char* qlin_status_string(qlin_status_t status) {
   }
 }
 
-int qlin_version(void) { return 102; }
+int qlin_version(void) { return 103; }
 
 }  // extern "C"

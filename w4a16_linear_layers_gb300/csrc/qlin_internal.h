@@ -19,15 +19,17 @@ struct DeviceInfo {
 // Returns the cached info of the current device (nullptr if no device).
 const DeviceInfo* current_device();
 
-cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, int8_t* q, float* s,
-                             cudaStream_t stream);
+// The act-quant producers write the codes q as int8, or (c16) as the same
+// integers in fp16 [M, K].
+cudaError_t launch_act_quant(const uint16_t* x, int64_t M, int64_t K, void* q, bool c16,
+                             float* s, cudaStream_t stream);
 
 cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
-                                 int64_t K, int8_t* q, float* s, uint16_t* y, int* err,
+                                 int64_t K, void* q, bool c16, float* s, uint16_t* y, int* err,
                                  int sm_count, cudaStream_t stream);
 
-cudaError_t launch_silu_mul_quant(const uint16_t* gate_up, int64_t M, int64_t I, int8_t* q,
-                                  float* s, uint16_t* y, int* err, int sm_count,
+cudaError_t launch_silu_mul_quant(const uint16_t* gate_up, int64_t M, int64_t I, void* q,
+                                  bool c16, float* s, uint16_t* y, int* err, int sm_count,
                                   cudaStream_t stream);
 
 cudaError_t launch_pack(const int8_t* q, int64_t K, int64_t N, int bits, int32_t* qweight,
@@ -66,6 +68,9 @@ struct GemmArgs {
   int group_size = 128;
   // Weights in the tile layout (qweight is then unused), else nullptr.
   const int32_t* wtiles = nullptr;
+  // W8A8: act holds the codes as fp16 [M,K] (integers in [-127, 127])
+  // instead of int8.
+  bool act_c16 = false;
 };
 
 // Offset of the argmax keys (one per row, M <= 96) inside the fixed counter
@@ -88,7 +93,9 @@ struct GemmPlan {
   int64_t ctas;    // grid size
   int64_t band;    // banded whole-tile schedule: token tiles per band (0: stream-K)
   size_t counter_bytes;
-  size_t act_offset;     // fp16 image of the W8A8 activations (token tiles >= 64)
+  size_t act_offset;     // W8A8 activations in the other code width: the fp16
+                         // image of int8 codes (token tiles >= 64) or the int8
+                         // codes of fp16 ones (token tiles <= 32)
   size_t workspace_bytes;
 };
 

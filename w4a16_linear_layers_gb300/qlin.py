@@ -34,7 +34,11 @@ EXPORTS = (
     "qlin_act_quant_i8",
     "qlin_rmsnorm_act_quant_i8",
     "qlin_silu_mul_act_quant_i8",
+    "qlin_act_quant_c16",
+    "qlin_rmsnorm_act_quant_c16",
+    "qlin_silu_mul_act_quant_c16",
     "qlin_gemm_w8a8_gs128",
+    "qlin_gemm_w8a8_gs128_c16",
     "qlin_gemm_w8a8_gs128_noalloc",
     "qlin_gemm_w4a16_g128",
     "qlin_gemm_w8a8_gs128_tiled",
@@ -86,7 +90,11 @@ def load():
             "qlin_act_quant_i8": ([P, I64, I64, P, P, P], I),
             "qlin_rmsnorm_act_quant_i8": ([P, P, ctypes.c_float, I64, I64, P, P, P, P], I),
             "qlin_silu_mul_act_quant_i8": ([P, I64, I64, P, P, P, P], I),
+            "qlin_act_quant_c16": ([P, I64, I64, P, P, P], I),
+            "qlin_rmsnorm_act_quant_c16": ([P, P, ctypes.c_float, I64, I64, P, P, P, P], I),
+            "qlin_silu_mul_act_quant_c16": ([P, I64, I64, P, P, P, P], I),
             "qlin_gemm_w8a8_gs128": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
+            "qlin_gemm_w8a8_gs128_c16": ([P, P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_gemm_w8a8_gs128_noalloc": ([P, P, P, P, I64, I64, I64, P, P], I),
             "qlin_gemm_w4a16_g128": ([P, P, P, I64, I64, I64, P, P, SZ, P], I),
             "qlin_gemm_w8a16": ([P, P, P, I64, I64, I64, I, P, P, SZ, P], I),
@@ -149,30 +157,52 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int) -> None:
 
 # ------------------------------------------------------------------- calls
 
-def act_quant_i8(x: torch.Tensor, q: torch.Tensor | None = None, s_a: torch.Tensor | None = None,
-                 stream=None):
-    """x bf16 [M,K] -> (q int8 [M,K], s_a fp32 [M])."""
-    _need(x, "x", torch.bfloat16, 2)
-    M, K = x.shape
+def _quant_outputs(M, K, device, q, s_a, code_dtype=torch.int8):
     if q is None:
-        q = torch.empty((M, K), dtype=torch.int8, device=x.device)
-    if s_a is None:
-        s_a = torch.empty((M,), dtype=torch.float32, device=x.device)
-    _need(q, "q", torch.int8, 2)
-    _need(s_a, "s_a", torch.float32, 1)
-    _check(load().qlin_act_quant_i8(_ptr(x), M, K, _ptr(q), _ptr(s_a), _stream_handle(stream)))
-    return q, s_a
-
-
-def _quant_outputs(M, K, device, q, s_a):
-    if q is None:
-        q = torch.empty((M, K), dtype=torch.int8, device=device)
+        q = torch.empty((M, K), dtype=code_dtype, device=device)
     if s_a is None:
         s_a = torch.empty((M,), dtype=torch.float32, device=device)
-    _need(q, "q", torch.int8, 2)
+    _need(q, "q", code_dtype, 2)
     _need(s_a, "s_a", torch.float32, 1)
     if tuple(q.shape) != (M, K) or tuple(s_a.shape) != (M,):
         raise ValueError("q must be [M, K] and s_a [M]")
+    return q, s_a
+
+
+def _act_quant(fn, code_dtype, x, q, s_a, stream):
+    _need(x, "x", torch.bfloat16, 2)
+    M, K = x.shape
+    q, s_a = _quant_outputs(M, K, x.device, q, s_a, code_dtype)
+    _check(fn(_ptr(x), M, K, _ptr(q), _ptr(s_a), _stream_handle(stream)))
+    return q, s_a
+
+
+def act_quant_i8(x: torch.Tensor, q: torch.Tensor | None = None, s_a: torch.Tensor | None = None,
+                 stream=None):
+    """x bf16 [M,K] -> (q int8 [M,K], s_a fp32 [M])."""
+    return _act_quant(load().qlin_act_quant_i8, torch.int8, x, q, s_a, stream)
+
+
+def act_quant_c16(x: torch.Tensor, q: torch.Tensor | None = None, s_a: torch.Tensor | None = None,
+                  stream=None):
+    """act_quant_i8 with the codes as fp16: -> (q fp16 [M,K] holding the same
+    integers, s_a fp32 [M])."""
+    return _act_quant(load().qlin_act_quant_c16, torch.float16, x, q, s_a, stream)
+
+
+def _rmsnorm_act_quant(fn, code_dtype, x, gamma, eps, q, s_a, y, stream):
+    _need(x, "x", torch.bfloat16, 2)
+    _need(gamma, "gamma", torch.bfloat16, 1)
+    M, K = x.shape
+    if tuple(gamma.shape) != (K,):
+        raise ValueError("gamma must be [K]")
+    q, s_a = _quant_outputs(M, K, x.device, q, s_a, code_dtype)
+    if y is not None:
+        _need(y, "y", torch.bfloat16, 2)
+        if tuple(y.shape) != (M, K):
+            raise ValueError("y must be [M, K]")
+    _check(fn(_ptr(x), _ptr(gamma), float(eps), M, K, _ptr(q), _ptr(s_a),
+              _ptr(y) if y is not None else None, _stream_handle(stream)))
     return q, s_a
 
 
@@ -181,19 +211,29 @@ def rmsnorm_act_quant_i8(x: torch.Tensor, gamma: torch.Tensor, eps: float, q=Non
     """RMSNorm of x bf16 [M,K] with weight gamma bf16 [K], then per-token INT8
     act-quant -> (q int8 [M,K], s_a fp32 [M]).  If y (bf16 [M,K]) is given
     the norm's bf16 output is written there too."""
-    _need(x, "x", torch.bfloat16, 2)
-    _need(gamma, "gamma", torch.bfloat16, 1)
-    M, K = x.shape
-    if tuple(gamma.shape) != (K,):
-        raise ValueError("gamma must be [K]")
-    q, s_a = _quant_outputs(M, K, x.device, q, s_a)
+    return _rmsnorm_act_quant(load().qlin_rmsnorm_act_quant_i8, torch.int8, x, gamma, eps, q, s_a,
+                              y, stream)
+
+
+def rmsnorm_act_quant_c16(x: torch.Tensor, gamma: torch.Tensor, eps: float, q=None, s_a=None,
+                          y=None, stream=None):
+    """rmsnorm_act_quant_i8 with the codes as fp16 (q fp16 [M,K])."""
+    return _rmsnorm_act_quant(load().qlin_rmsnorm_act_quant_c16, torch.float16, x, gamma, eps, q,
+                              s_a, y, stream)
+
+
+def _silu_mul_act_quant(fn, code_dtype, gate_up, q, s_a, y, stream):
+    _need(gate_up, "gate_up", torch.bfloat16, 2)
+    M, I2 = gate_up.shape
+    if I2 % 2:
+        raise ValueError("gate_up must have an even number of columns")
+    q, s_a = _quant_outputs(M, I2 // 2, gate_up.device, q, s_a, code_dtype)
     if y is not None:
         _need(y, "y", torch.bfloat16, 2)
-        if tuple(y.shape) != (M, K):
-            raise ValueError("y must be [M, K]")
-    _check(load().qlin_rmsnorm_act_quant_i8(_ptr(x), _ptr(gamma), float(eps), M, K, _ptr(q),
-                                            _ptr(s_a), _ptr(y) if y is not None else None,
-                                            _stream_handle(stream)))
+        if tuple(y.shape) != (M, I2 // 2):
+            raise ValueError("y must be [M, I]")
+    _check(fn(_ptr(gate_up), M, I2 // 2, _ptr(q), _ptr(s_a), _ptr(y) if y is not None else None,
+              _stream_handle(stream)))
     return q, s_a
 
 
@@ -201,19 +241,14 @@ def silu_mul_act_quant_i8(gate_up: torch.Tensor, q=None, s_a=None, y=None, strea
     """SiLU(gate) * up of gate_up bf16 [M, 2I] (gate columns first), then
     per-token INT8 act-quant -> (q int8 [M,I], s_a fp32 [M]).  If y (bf16
     [M,I]) is given the activation's bf16 output is written there too."""
-    _need(gate_up, "gate_up", torch.bfloat16, 2)
-    M, I2 = gate_up.shape
-    if I2 % 2:
-        raise ValueError("gate_up must have an even number of columns")
-    q, s_a = _quant_outputs(M, I2 // 2, gate_up.device, q, s_a)
-    if y is not None:
-        _need(y, "y", torch.bfloat16, 2)
-        if tuple(y.shape) != (M, I2 // 2):
-            raise ValueError("y must be [M, I]")
-    _check(load().qlin_silu_mul_act_quant_i8(_ptr(gate_up), M, I2 // 2, _ptr(q), _ptr(s_a),
-                                             _ptr(y) if y is not None else None,
-                                             _stream_handle(stream)))
-    return q, s_a
+    return _silu_mul_act_quant(load().qlin_silu_mul_act_quant_i8, torch.int8, gate_up, q, s_a, y,
+                               stream)
+
+
+def silu_mul_act_quant_c16(gate_up: torch.Tensor, q=None, s_a=None, y=None, stream=None):
+    """silu_mul_act_quant_i8 with the codes as fp16 (q fp16 [M,I])."""
+    return _silu_mul_act_quant(load().qlin_silu_mul_act_quant_c16, torch.float16, gate_up, q, s_a,
+                               y, stream)
 
 
 def workspace_bytes(M: int, N: int, K: int) -> int:
@@ -250,12 +285,8 @@ def _workspace(ws, M, N, K, device):
     return ws
 
 
-def gemm_w8a8_gs128(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
-                    scales: torch.Tensor, y: torch.Tensor | None = None, workspace=None,
-                    stream=None) -> torch.Tensor:
-    """q_a int8 [M,K], s_a fp32 [M], qweight int32 [K/4,N], scales fp16 [K/128,N]
-    -> y bf16 [M,N]."""
-    _need(q_a, "q_a", torch.int8, 2)
+def _gemm_w8a8(fn, code_dtype, q_a, s_a, qweight, scales, y, workspace, stream):
+    _need(q_a, "q_a", code_dtype, 2)
     _need(s_a, "s_a", torch.float32, 1)
     _need(qweight, "qweight", torch.int32, 2)
     _need(scales, "scales", torch.float16, 2)
@@ -267,9 +298,27 @@ def gemm_w8a8_gs128(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
         y = torch.empty((M, N), dtype=torch.bfloat16, device=q_a.device)
     _need(y, "y", torch.bfloat16, 2)
     ws = _workspace(workspace, M, N, K, q_a.device)
-    _check(load().qlin_gemm_w8a8_gs128(_ptr(q_a), _ptr(s_a), _ptr(qweight), _ptr(scales), M, N, K,
-                                       _ptr(y), _ptr(ws), ws.numel(), _stream_handle(stream)))
+    _check(fn(_ptr(q_a), _ptr(s_a), _ptr(qweight), _ptr(scales), M, N, K, _ptr(y), _ptr(ws),
+              ws.numel(), _stream_handle(stream)))
     return y
+
+
+def gemm_w8a8_gs128(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
+                    scales: torch.Tensor, y: torch.Tensor | None = None, workspace=None,
+                    stream=None) -> torch.Tensor:
+    """q_a int8 [M,K], s_a fp32 [M], qweight int32 [K/4,N], scales fp16 [K/128,N]
+    -> y bf16 [M,N]."""
+    return _gemm_w8a8(load().qlin_gemm_w8a8_gs128, torch.int8, q_a, s_a, qweight, scales, y,
+                      workspace, stream)
+
+
+def gemm_w8a8_gs128_c16(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
+                        scales: torch.Tensor, y: torch.Tensor | None = None, workspace=None,
+                        stream=None) -> torch.Tensor:
+    """gemm_w8a8_gs128 with the activation codes as fp16 (q_a fp16 [M,K], the
+    output of the *_c16 producers)."""
+    return _gemm_w8a8(load().qlin_gemm_w8a8_gs128_c16, torch.float16, q_a, s_a, qweight, scales,
+                      y, workspace, stream)
 
 
 def gemm_w8a8_gs128_noalloc(q_a: torch.Tensor, s_a: torch.Tensor, qweight: torch.Tensor,
