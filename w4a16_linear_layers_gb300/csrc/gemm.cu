@@ -107,11 +107,16 @@ struct Cfg {
   // warps 12..: epilogue, kEpiPerQ warps per TMEM lane quarter, each
   //              draining T / kEpiPerQ token columns of the accumulator, all
   //              of them with one batch of TMEM loads (at most 32 columns, so
-  //              the loaded values and the running sums fit in registers)
+  //              the loaded values and the running sums fit in registers).
+  //              W8A8 token tiles of 32 and fewer take one warp per quarter:
+  //              512 threads leave 128 registers a thread instead of 96 (no
+  //              spills) and four fewer warps compete for issue slots, which
+  //              ran the decode shapes 4-5% faster; the weight-only formats,
+  //              whose epilogue drains once per segment, measured no gain.
   static constexpr int kConvWarp0 = 4;
   static constexpr int kConvWarps = 8;
   static constexpr int kEpiWarp0 = 12;
-  static constexpr int kEpiPerQ = T > 64 ? 3 : 2;
+  static constexpr int kEpiPerQ = T > 64 ? 3 : (T <= 32 && !kWO ? 1 : 2);
   static constexpr int kEpiWarps = 4 * kEpiPerQ;
   static constexpr int kConvThreads = 32 * kConvWarps;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
