@@ -277,14 +277,19 @@ __device__ __forceinline__ uint4 norm8(uint4 x, uint4 g, const RowScale& rs) {
 // programming guide's maximum-error tables), plus four roundings, the fp32
 // value is within 12 ulps of the exact one; within 16 ulps of a bf16 halfway
 // point it is formed again in fp64 as g / (1 + exp(-g)) * u.
+// The fp64 form, out of line: it is rare (a window of 32 fp32 ulps in
+// 65536), and inlined into every unrolled element it would multiply the
+// kernel's code size.
+__device__ __noinline__ uint32_t silu_mul_f64(float g, float u) {
+  const double gd = static_cast<double>(g);
+  return f64_to_bf16_bits(gd / (1.0 + exp(-gd)) * static_cast<double>(u));
+}
+
 __device__ __forceinline__ uint32_t silu_mul1(float g, float u) {
   const float e = expf(-fabsf(g));
   const float sig = __fdividef(g >= 0.0f ? 1.0f : e, __fadd_rn(1.0f, e));
   const float v = __fmul_rn(__fmul_rn(g, sig), u);
-  if (near_bf16_half(__float_as_uint(v), 16u)) {
-    const double gd = static_cast<double>(g);
-    return f64_to_bf16_bits(gd / (1.0 + exp(-gd)) * static_cast<double>(u));
-  }
+  if (near_bf16_half(__float_as_uint(v), 16u)) return silu_mul_f64(g, u);
   return bf16_bits_rn(v);
 }
 
