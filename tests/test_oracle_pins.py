@@ -664,3 +664,15 @@ def test_pack_tiles_hand_words(oracle_lib):
     assert t[base + 5 * 128 + 1] == 37 * 1000 + 129
     assert t[base + 5 * 128 + 2] == 0
     assert t[(0 * 2 + 1) * 32 * 128 + 0 * 128 + 127] == 32 * 1000 + 127     # tile (0, 1)
+
+
+# ------------------------------------------------------------ input generator
+
+@pytest.mark.parametrize("shape,lo,hi", [((64, 130), -127, 127), ((257,), -7, 7), ((3, 5, 7), -127, 127)])
+def test_device_draw_equals_the_host_draw(shape, lo, hi):
+    """synth.randint_device (torch, used for gigabyte weight matrices) draws
+    the host generator's integers bit for bit; run here with torch on the
+    CPU, which computes the same int64 arithmetic."""
+    host = synth.randint(7, "pins/device_draw", shape, lo, hi)
+    dev = synth.randint_device(7, "pins/device_draw", shape, lo, hi, "cpu")
+    assert np.array_equal(dev.numpy().reshape(host.shape), host)
