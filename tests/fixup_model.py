@@ -1,16 +1,21 @@
 """A model of the GEMM's cross-block split-tile protocol, for randomized checking.
 
 Stream-K gives block c the steps [c*W//C, (c+1)*W//C) of the W = tiles * G
-(tile, group) steps.  A tile whose G steps fall to several blocks is split:
-each contributor publishes its fp32 partial to its own workspace slot (slot 0
-for the tile its range starts in, slot 1 for the tile it ends in), then
-arrives on an arrival counter with an acquire-release atomic add.  The counter
-of a split tile is the one of its first contributing block (a block is the
-first contributor of at most one split tile: the tile its range ends in).
-After its last step a block looks at the counts its arrivals returned: the
-block whose arrival completed the count is the last one, reads every
-contributor's partial (ascending block order), writes the tile's output and
-sets the counter back to zero for the next call.  Consecutive calls that share
+(tile, group) steps.  A tile whose G steps fall to several blocks is split.
+The counter of a split tile is the one of its first contributing block (a
+block is the first contributor of at most one split tile: the tile its range
+ends in).  A contributor whose range starts in the tile (slot 0: the tile's
+later groups, or all of a block whose range lies inside the tile) publishes
+its fp32 partial to its workspace slot, then arrives on the counter with an
+acquire-release atomic add, and looks at the count it got only after its
+last step.  The first contributor, whose range ends in the tile (slot 1),
+arrives only after its last step: if its arrival completes the count it
+finishes the tile from its own registers and the others' partials; if not,
+it publishes its partial to slot 1 and then adds a published flag (bit 16)
+to the counter with release semantics.  The block whose arrival completed
+the count reads every contributor's partial in ascending block order -- the
+first contributor's slot 1 only once the flag is set -- writes the tile's
+output and sets the counter back to zero for the next call.  Consecutive calls that share
 the workspace are ordered by the grid dependency: a block writes partials,
 counters or outputs only once the previous call has completed.
 
@@ -23,11 +28,16 @@ visible, per tick.
 The checker reports a finisher reading a partial that is not the current
 call's partial of that tile, a split tile finished zero or several times, an
 output written twice, a counter left non-zero after a call, two split tiles
-sharing a counter, and an agent that can never run.
+sharing a counter, and an agent that can never run.  A wait on the flag runs
+forever in the model when nothing will set it (a deadlock is then reported
+as no progress).
 
 Only tests use this module; it restates the protocol, not the kernel code.
 """
 import random
+
+FLAG = 1 << 16     # published-partial flag of the first contributor
+MASK = FLAG - 1
 
 
 def ranges(W, C):
@@ -110,6 +120,10 @@ def _block(sim, call, c, W, G, C, opts, done):
             continue
         slot = 0 if t == first_tile else 1
         c_first = block_of_step(t * G, W, C)
+        if slot == 1 and not opts.get("publish_first_everywhere"):
+            pend.append((t, None, "end"))     # arrives after its last step
+            yield "step"
+            continue
         if opts.get("arrive_before_publish"):
             old = sim.mem.get(("cnt", c_first), 0)
             sim.mem[("cnt", c_first)] = old + 1
@@ -122,18 +136,45 @@ def _block(sim, call, c, W, G, C, opts, done):
                 sim.flush(me)          # release: the partial before the count
             old = sim.mem.get(("cnt", c_first), 0)
             sim.mem[("cnt", c_first)] = old + 1
-        pend.append((t, old))
+        pend.append((t, old, "start"))
         yield "step"
-    for t, old in pend:
+    # the end piece first (its partial is still in registers), then the start
+    # piece
+    pend.sort(key=lambda e: e[2] != "end")
+    for t, old, kind in pend:
         c_first = block_of_step(t * G, W, C)
         c_last = block_of_step(t * G + G - 1, W, C)
-        if old != c_last - c_first:
+        own = None
+        if kind == "end":
+            sim.flush(me)                              # acquire-release arrival
+            old = sim.mem.get(("cnt", c_first), 0)
+            sim.mem[("cnt", c_first)] = old + 1
+            yield "step"
+            s_own = segments(*ranges(W, C)[c], G)[-1]
+            if (old & MASK) != c_last - c_first:
+                sim.store(me, ("part", c, 1), (call, t, s_own[1], s_own[2]))
+                yield "step"
+                if not opts.get("flag_before_flush"):
+                    sim.flush(me)                      # release: the partial before the flag
+                sim.mem[("cnt", c_first)] = sim.mem.get(("cnt", c_first), 0) + FLAG
+                yield "step"
+                continue
+            own = (call, t, s_own[1], s_own[2])
+        elif (old & MASK) != c_last - c_first:
             continue
         # the last arrival: every contributor's partial, ascending blocks
         covered = []
         for cc in range(c_first, c_last + 1):
             slot = 0 if (ranges(W, C)[cc][0] // G) == t else 1
-            v = sim.mem.get(("part", cc, slot))
+            if cc == c and own is not None:
+                v = own
+            else:
+                if slot == 1 and not opts.get("publish_first_everywhere") \
+                        and not opts.get("skip_flag_wait"):
+                    # the first contributor publishes after its arrival
+                    while not (sim.mem.get(("cnt", c_first), 0) & FLAG):
+                        yield "wait"
+                v = sim.mem.get(("part", cc, slot))
             if v is None or v[0] != call or v[1] != t:
                 sim.fail(f"call {call}: block {c} finishing tile {t} read block {cc}'s "
                          f"slot {slot} = {v}")

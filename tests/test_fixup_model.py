@@ -1,7 +1,9 @@
 """Randomized checks of the GEMM's cross-block split-tile protocol (CPU only).
 
 `fixup_model` restates how blocks publish split-tile partials, count their
-arrivals, finish a tile in the last arriving block and reset its counter;
+arrivals (the first contributor of a tile after its last step, publishing
+only if another block finishes the tile), finish a tile in the last arriving
+block and reset its counter;
 these tests run several consecutive calls sharing one workspace under random
 interleavings and random store visibility, over stream-K shapes like the
 decode layers' (more blocks than tiles: tiles split across several blocks;
@@ -30,6 +32,24 @@ def test_block_of_step_closed_form():
 def test_split_tiles_finish_once_with_every_partial(W, G, C):
     for seed in range(6 if W > 2000 else 30):
         assert fm.run(W, G, C, calls=3, seed=seed) is None
+
+
+@pytest.mark.parametrize("W,G,C", SHAPES[3:])
+def test_publishing_before_every_arrival_is_also_correct(W, G, C):
+    """The plainer protocol (every contributor publishes, then arrives)."""
+    for seed in range(20):
+        assert fm.run(W, G, C, calls=2, seed=seed, publish_first_everywhere=True) is None
+
+
+@pytest.mark.parametrize("flaw", ["skip_flag_wait", "flag_before_flush"])
+def test_reading_the_first_contributors_partial_before_its_flag_is_caught(flaw):
+    """When the first contributor arrives before another block completes the
+    count, it publishes afterwards: a finisher that does not wait for the
+    published flag, or a flag raised before the partial is visible, reads a
+    stale slot."""
+    bad = [fm.run(W, G, C, calls=2, seed=s, **{flaw: True})
+           for W, G, C in SHAPES[3:] for s in range(60)]
+    assert any(r is not None and "read block" in r for r in bad)
 
 
 @pytest.mark.parametrize("flaw", ["arrive_before_publish", "relaxed_arrival"])

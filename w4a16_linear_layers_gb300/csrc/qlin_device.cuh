@@ -212,6 +212,18 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
   return old;
 }
 
+// int reduction (no result) with release semantics at GPU scope.
+__device__ __forceinline__ void red_add_release_gpu(int* addr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+// int load with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int* addr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
