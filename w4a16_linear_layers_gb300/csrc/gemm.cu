@@ -13,7 +13,7 @@
 // most 128*127*127 < 2^24, so the fp32 accumulator holds the exact integer
 // group partial.
 //
-// Structure (one persistent block of 640 or 768 threads per SM):
+// Structure (one persistent block of 512, 640 or 768 threads per SM):
 //   * the output is cut into tiles of 128 features x T tokens; the MMA runs
 //     with the weights as operand A (128 rows = features, converted by
 //     threads straight into TMEM) and the tokens as operand B (T columns,
@@ -23,19 +23,24 @@
 //     tokens of tiles up to 32 land as int8 tiles and the converter group of
 //     the step expands them exactly to fp16 beside the weights it converts
 //     (half the bytes from L2, and no extra kernel between act-quant and the
-//     GEMM); larger W8A8 tiles read an exact fp16 image written by a small
-//     pre-pass kernel;
+//     GEMM); larger W8A8 tiles read 16-bit codes by TMA: the caller's fp16
+//     codes, or an exact fp16 image of int8 codes written by a small pre-pass
+//     kernel;
 //   * the work is the list of (tile, group) steps; block c takes the
 //     contiguous range [c*W/C, (c+1)*W/C) of the W steps (stream-K), so every
 //     SM gets the same amount of weight stream whatever the shape;
 //   * a tile split between blocks is finished by the last block to arrive on
 //     its counter, which sums the per-block fp32 partials in ascending block
-//     order (deterministic, no spin waits);
+//     order (deterministic); at W8A8 tiles of 64 and more the tile's first
+//     contributor arrives only after its last step and, when it is not the
+//     last, publishes afterwards, so the finisher waits (bounded) for its
+//     flag -- on a block that has already arrived;
 //   * roles: warp 0 streams weights by TMA, warp 2 streams activations and
 //     group scales, warps 1 and 3 issue the MMAs of alternate steps (one
 //     thread's issue rate is below what the weight stream needs), warps 4-11
 //     convert weights into TMEM (and W8A8 tokens into fp16), warps 12 and
-//     up drain TMEM (two per TMEM lane quarter, three at 96-token tiles).
+//     up drain TMEM (one per TMEM lane quarter for W8A8 tiles of 32 and
+//     fewer, two otherwise, three at 96-token tiles).
 //
 // W8A8 per group g:  D = A_g * B_g (exact integers), then acc = fma(D, s_w, acc)
 // in the epilogue, ascending g; at the end y = bf16(acc * s_a).
@@ -134,9 +139,9 @@ struct Cfg {
   //   (freed by the converters) and the converter group of the step expands
   //   them exactly to fp16 in the operand slot that pairs with its A buffer.
   //   W8A8, T >= 64: that expansion would add 24-36 KB of shared-memory
-  //   traffic and a quarter of the converters' instructions per step; a
-  //   pre-pass kernel writes the exact fp16 image once and its tiles land
-  //   like W4A16's.
+  //   traffic and a quarter of the converters' instructions per step; the
+  //   caller's fp16 codes, or an exact fp16 image written once by a pre-pass
+  //   kernel, land like W4A16's tiles.
   // The first ring in each case is deep enough to cover the L2 latency seen
   // while the weight stream keeps HBM busy.
   static constexpr uint32_t kStageBytes = kWBytes;
