@@ -14,7 +14,9 @@
 // from L2).  The row maximum of |x| is reduced with warp shuffles and one
 // shared-memory step; s = amax / 127 is an IEEE fp32 divide, and the codes are
 // those of rint(x / s) with an IEEE divide (quant1y), written as 8-byte
-// stores.  The producer kernels are described at "fused producers" below.
+// stores of int8, or for the _c16 calls as the same integers in fp16 (16-byte
+// stores), the W8A8 GEMM's tensor-core operand type.  The producer kernels
+// are described at "fused producers" below.
 #include <cuda_bf16.h>
 
 #include <mutex>
